@@ -1,0 +1,37 @@
+"""CPU oracle for the greedy DFlash draft-and-verify round.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference arm of ``bench.py`` may import, call or execute
+anything in this package.  The CUDA library never does, and nothing here
+imports the library: the two share only the seeded inputs from ``synth``.
+
+Contents
+--------
+model    fp64 target decoder, context fusion, KV injection, block drafter.
+spec     prefill / draft / verify / accept loop, plain AR greedy decode,
+         planted proposals that fix the number of accepted drafts.
+metrics  acceptance length, cycle latency, speedup, memory accounting,
+         context-layer selection.
+
+Pins (checked by ``tests/test_oracle_*.py`` against the pages and the
+mathematics, not against this code):
+
+* speculative greedy output == plain AR greedy output (losslessness),
+  for several block sizes, batch shapes and proposers, including block 1;
+* the drafter's incremental context cache == a from-scratch recomputation of
+  every context feature and key/value from the committed sequence;
+* the verify pass with cache rollback == a fresh causal forward of the
+  committed sequence;
+* brute-force attention (scalar loops) for the causal and the bidirectional
+  masks; closed forms of RMSNorm, RoPE and SiLU;
+* acceptance against its characterisation, exhaustively on tiny inputs;
+  planted proposals accept exactly the planted count;
+* printed worked values of the review's eq. 3, eq. 4/5 and eq. 11 and the
+  context-layer lists of the workloads.
+
+Parity unpinned: the drafter's numerical output as a whole.  No trained draft
+weights exist here, so nothing outside this code fixes what a random-init
+drafter should propose beyond the structural pins above (context injection,
+bidirectional attention, cache reuse and immutability).
+"""
+from . import metrics, model, spec  # noqa: F401
