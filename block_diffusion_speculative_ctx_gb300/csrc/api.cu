@@ -1,0 +1,1007 @@
+// C-ABI layer: session state, weight packing, and the orchestration of
+// prefill, draft_block, verify and generate on one CUDA stream.
+//
+// The round follows the greedy decoding-round pseudocode of "DFlash: Block
+// Diffusion for Flash Speculative Decoding" (Method, Inference §4.1) and the
+// verification rule of "DFlash: Why a Diffusion Drafter Can Accelerate an
+// Autoregressive Model" (§4.1, Algorithm 1).  Every arithmetic step runs in
+// the kernels of this library; the host only sequences launches, copies
+// tokens, and keeps lengths for capacity checks.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "dflash.h"
+#include "launch.h"
+
+using namespace dfl;
+
+namespace {
+
+constexpr int PAGE_TOKENS = 64;
+constexpr int PAGE_SHIFT = 6;
+constexpr int PREFILL_CHUNK = 2048;
+constexpr size_t ATTN_WS_BYTES = 64ull << 20;
+
+enum State { ST_EMPTY = 0, ST_READY = 1, ST_DRAFTED = 2 };
+
+thread_local std::string g_init_error;
+
+struct LayerW {
+    void* wqkv = nullptr;   // [(H + 2 Hkv) hd, d]: rows wq, wk, wv
+    void* wo = nullptr;     // [d, H hd]
+    void* wgu = nullptr;    // [2F, d]: rows w_gate, w_up
+    void* wdown = nullptr;  // [d, F]
+    float* attn_norm = nullptr;
+    float* mlp_norm = nullptr;
+    float* q_norm = nullptr;
+    float* k_norm = nullptr;
+};
+
+}  // namespace
+
+struct dflash_ctx {
+    dflash_config cfg;
+    cudaStream_t stream = nullptr;
+    std::string err;
+    std::vector<void*> allocs;
+    long long launches = 0;
+    size_t esz = 4;  // element size of the storage type
+
+    int d, H, Hkv, hd, F, V, Lt, Ld, B, k, qd, kvd, qkv_n, max_seq;
+    int ctx_slot[64];  // target layer -> index in ctx_layer_ids or -1
+
+    std::vector<LayerW> tl, dl;
+    void* embed = nullptr;
+    void* head = nullptr;
+    void* fc = nullptr;
+    float* final_norm = nullptr;
+    float* fc_norm = nullptr;
+    float* draft_norm = nullptr;
+
+    KVLayout kv;
+    void *tK = nullptr, *tV = nullptr, *dK = nullptr, *dV = nullptr;
+    int* page_table = nullptr;
+    float2* rope = nullptr;
+
+    int R = 0;  // row capacity
+    float* x = nullptr;
+    void* xn = nullptr;
+    float* qkv = nullptr;
+    void* q = nullptr;
+    void* att = nullptr;
+    float* gu = nullptr;
+    void* hmid = nullptr;
+    void* stage = nullptr;
+    float* fcout = nullptr;
+    void* feat = nullptr;
+    float* kvout = nullptr;
+    float* logits = nullptr;
+    int* tokens = nullptr;
+    int* row_seq = nullptr;
+    int* row_pos = nullptr;
+    int* ctx_row_seq = nullptr;
+    int* ctx_row_pos = nullptr;
+    int* n = nullptr;
+    int* anchor = nullptr;
+    int* proposal = nullptr;
+    int* posterior = nullptr;
+    int* argbuf = nullptr;
+    int* accepted = nullptr;
+    int* bonus = nullptr;
+    int* drafts = nullptr;
+    uint32_t* errw = nullptr;
+    float* attn_ws = nullptr;
+    float* keep_prefill = nullptr;
+    float* keep_draft = nullptr;
+    float* keep_verify = nullptr;
+    float* keep_hidden = nullptr;
+
+    int batch = 0;
+    int state = ST_EMPTY;
+    bool pending_append = false;
+    std::vector<int> n_upper;  // host upper bound of n (exact after a synchronising verify)
+
+    dflash_stats stats;
+    cudaEvent_t ev[4];
+    bool events = false;
+
+    // kernel-class profile (DFLASH_FLAG_PROFILE)
+    struct ProfRec {
+        int kind, e0, e1;
+        long long launches;
+        double bytes, flops;
+    };
+    bool profiling = false;
+    std::vector<cudaEvent_t> prof_ev;
+    int prof_next = 0;
+    std::vector<ProfRec> prof_pending;
+    dflash_profile_entry prof_acc[DFLASH_K_COUNT];
+
+    Launch L() { return Launch{stream, &launches}; }
+
+    dflash_status fail(dflash_status s, const char* fmt, ...) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        err = buf;
+        return s;
+    }
+};
+
+namespace {
+
+#define CUDA_TRY(ctx, call)                                                                   \
+    do {                                                                                      \
+        cudaError_t e_ = (call);                                                              \
+        if (e_ != cudaSuccess)                                                                \
+            return (ctx)->fail(DFLASH_E_CUDA, "%s: %s", #call, cudaGetErrorString(e_));      \
+    } while (0)
+
+void* dev_alloc(dflash_ctx* c, size_t bytes) {
+    if (bytes == 0) bytes = 16;
+    void* p = nullptr;
+    if (c->cfg.alloc) {
+        p = c->cfg.alloc(bytes, c->cfg.alloc_user);
+    } else if (cudaMalloc(&p, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        p = nullptr;
+    }
+    if (p) c->allocs.push_back(p);
+    return p;
+}
+
+bool is_device_ptr(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+template <typename T>
+T* elem(void* base, size_t offset_elems) {
+    return reinterpret_cast<T*>(base) + offset_elems;
+}
+
+dflash_status validate(const dflash_config* c, std::string& why) {
+    char buf[256];
+    auto bad = [&](const char* m) {
+        why = m;
+        return DFLASH_E_INVAL;
+    };
+    if (c->dtype != DFLASH_DTYPE_F32 && c->dtype != DFLASH_DTYPE_BF16) return bad("dtype must be F32 or BF16");
+    if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
+    if (c->d_model <= 0 || c->d_model % 64) return bad("d_model must be a positive multiple of 64");
+    if (c->ffn <= 0 || c->ffn % 64) return bad("ffn must be a positive multiple of 64");
+    if (c->n_heads <= 0 || c->n_kv_heads <= 0 || c->n_heads % c->n_kv_heads) return bad("n_heads % n_kv_heads != 0");
+    if (c->n_heads / c->n_kv_heads > 64) return bad("more than 64 query heads per KV head");
+    if (c->vocab <= 1) return bad("vocab must be > 1");
+    if (c->target_layers <= 0 || c->target_layers > 64) return bad("target_layers must be in [1, 64]");
+    if (c->draft_layers <= 0 || c->draft_layers > 64) return bad("draft_layers must be in [1, 64]");
+    if (c->block_size < 1 || c->block_size > 32) return bad("block_size must be in [1, 32]");
+    if (c->n_ctx_layers < 1 || c->n_ctx_layers > DFLASH_MAX_CTX_LAYERS) return bad("n_ctx_layers out of range");
+    for (int i = 0; i < c->n_ctx_layers; ++i)
+        if (c->ctx_layer_ids[i] < 0 || c->ctx_layer_ids[i] >= c->target_layers) {
+            snprintf(buf, sizeof buf, "ctx_layer_ids[%d] = %d outside [0, target_layers)", i, c->ctx_layer_ids[i]);
+            why = buf;
+            return DFLASH_E_INVAL;
+        }
+    for (int i = 0; i < c->n_ctx_layers; ++i)
+        for (int j = 0; j < i; ++j)
+            if (c->ctx_layer_ids[i] == c->ctx_layer_ids[j]) return bad("ctx_layer_ids must be distinct");
+    if (c->mask_token < 0 || c->mask_token >= c->vocab) return bad("mask_token outside [0, vocab)");
+    if (c->max_batch < 1 || c->max_batch > 1024) return bad("max_batch must be in [1, 1024]");
+    if (c->max_seq_len < c->block_size + 1) return bad("max_seq_len too small");
+    if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.0)) return bad("rms_eps and rope_theta must be positive");
+    if ((c->alloc == nullptr) != (c->free == nullptr)) return bad("alloc and free must both be set or both NULL");
+    if ((double)c->max_batch * c->block_size * 2 * c->ffn > 2e9) return bad("batch x block x ffn too large");
+    return DFLASH_OK;
+}
+
+// Copy a [rows, cols] device matrix into dst at row offset (element size esz).
+dflash_status copy_rows(dflash_ctx* c, void* dst, size_t row_off, const void* src, size_t rows, size_t cols) {
+    if (!src) return c->fail(DFLASH_E_INVAL, "a weight pointer is NULL");
+    CUDA_TRY(c, cudaMemcpyAsync((char*)dst + row_off * cols * c->esz, src, rows * cols * c->esz,
+                                cudaMemcpyDeviceToDevice, c->stream));
+    return DFLASH_OK;
+}
+
+dflash_status copy_norm(dflash_ctx* c, float** dst, const float* src, size_t n, bool optional) {
+    if (!src) {
+        if (optional) {
+            *dst = nullptr;
+            return DFLASH_OK;
+        }
+        return c->fail(DFLASH_E_INVAL, "a norm weight pointer is NULL");
+    }
+    *dst = (float*)dev_alloc(c, n * 4);
+    if (!*dst) return c->fail(DFLASH_E_NOMEM, "allocation of %zu bytes failed", n * 4);
+    CUDA_TRY(c, cudaMemcpyAsync(*dst, src, n * 4, cudaMemcpyDeviceToDevice, c->stream));
+    return DFLASH_OK;
+}
+
+dflash_status pack_layer(dflash_ctx* c, const dflash_layer_weights& w, LayerW& o, bool qk_norm) {
+    const size_t d = c->d, F = c->F, qd = c->qd, kvd = c->kvd;
+    o.wqkv = dev_alloc(c, (qd + 2 * kvd) * d * c->esz);
+    o.wo = dev_alloc(c, d * qd * c->esz);
+    o.wgu = dev_alloc(c, 2 * F * d * c->esz);
+    o.wdown = dev_alloc(c, d * F * c->esz);
+    if (!o.wqkv || !o.wo || !o.wgu || !o.wdown) return c->fail(DFLASH_E_NOMEM, "weight allocation failed");
+    dflash_status s;
+    if ((s = copy_rows(c, o.wqkv, 0, w.wq, qd, d))) return s;
+    if ((s = copy_rows(c, o.wqkv, qd, w.wk, kvd, d))) return s;
+    if ((s = copy_rows(c, o.wqkv, qd + kvd, w.wv, kvd, d))) return s;
+    if ((s = copy_rows(c, o.wo, 0, w.wo, d, qd))) return s;
+    if ((s = copy_rows(c, o.wgu, 0, w.w_gate, F, d))) return s;
+    if ((s = copy_rows(c, o.wgu, F, w.w_up, F, d))) return s;
+    if ((s = copy_rows(c, o.wdown, 0, w.w_down, d, F))) return s;
+    if ((s = copy_norm(c, &o.attn_norm, w.attn_norm, d, false))) return s;
+    if ((s = copy_norm(c, &o.mlp_norm, w.mlp_norm, d, false))) return s;
+    if (qk_norm) {
+        if ((s = copy_norm(c, &o.q_norm, w.q_norm, c->hd, false))) return s;
+        if ((s = copy_norm(c, &o.k_norm, w.k_norm, c->hd, false))) return s;
+    }
+    return DFLASH_OK;
+}
+
+// Device error word -> status (synchronises).
+dflash_status check_device(dflash_ctx* c) {
+    uint32_t e = 0;
+    CUDA_TRY(c, cudaMemcpyAsync(&e, c->errw, 4, cudaMemcpyDeviceToHost, c->stream));
+    CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+    if (e) {
+        CUDA_TRY(c, cudaMemsetAsync(c->errw, 0, 4, c->stream));
+        return c->fail(DFLASH_E_DEVICE_CHECK, "device-side check failed (code %u%s%s)", e,
+                       (e & ERR_TOKEN_RANGE) ? ": token id outside [0, vocab)" : "",
+                       (e & ERR_POSITION_RANGE) ? ": position beyond max_seq_len" : "");
+    }
+    return DFLASH_OK;
+}
+
+// Fold recorded event pairs into the per-class profile (synchronises).
+dflash_status prof_drain(dflash_ctx* c) {
+    if (c->prof_pending.empty()) return DFLASH_OK;
+    CUDA_TRY(c, cudaEventSynchronize(c->prof_ev[c->prof_pending.back().e1]));
+    for (const auto& r : c->prof_pending) {
+        float ms = 0.f;
+        CUDA_TRY(c, cudaEventElapsedTime(&ms, c->prof_ev[r.e0], c->prof_ev[r.e1]));
+        dflash_profile_entry& a = c->prof_acc[r.kind];
+        a.launches += r.launches;
+        a.ms += ms;
+        a.bytes += r.bytes;
+        a.flops += r.flops;
+    }
+    c->prof_pending.clear();
+    c->prof_next = 0;
+    return DFLASH_OK;
+}
+
+// Run f (which enqueues kernels of one class); with profiling on, bracket it
+// with events and remember its algorithmic bytes and flops.
+template <class F>
+void timed(dflash_ctx* c, int kind, double bytes, double flops, F&& f) {
+    if (!c->profiling) {
+        f();
+        return;
+    }
+    if (c->prof_next + 2 > (int)c->prof_ev.size()) prof_drain(c);
+    const int e0 = c->prof_next++, e1 = c->prof_next++;
+    const long long l0 = c->launches;
+    cudaEventRecord(c->prof_ev[e0], c->stream);
+    f();
+    cudaEventRecord(c->prof_ev[e1], c->stream);
+    c->prof_pending.push_back({kind, e0, e1, c->launches - l0, bytes, flops});
+}
+
+double gemm_bytes(const dflash_ctx* c, double M, double N, double K, bool acc) {
+    return N * K * c->esz + M * K * c->esz + M * N * 4.0 * (acc ? 2.0 : 1.0);
+}
+
+int attn_group_rows(int rows_per_seq, int g) {
+    int best = 1;
+    for (int r = 1; r <= rows_per_seq; ++r)
+        if (rows_per_seq % r == 0 && r * g <= 64) best = r;
+    return best;
+}
+
+// ------------------------------------------------------------ model passes
+template <typename T>
+struct Pass {
+    dflash_ctx* c;
+
+    KVLayout kvl() const { return c->kv; }
+
+    // Decoder layers over `rows` rows whose metadata is (row_seq, row_pos).
+    // target: causal attention over the target cache, capture of context layers
+    // into stage; draft: bidirectional attention over [context ; block].
+    void layers(bool target, int rows, const int* row_seq, const int* row_pos, int group_rows, int max_keys,
+                bool capture, double keys_total) {
+        Launch L = c->L();
+        const int nl = target ? c->Lt : c->Ld;
+        T* xn = (T*)c->xn;
+        const double R = rows, d = c->d, es = c->esz;
+        for (int l = 0; l < nl; ++l) {
+            const LayerW& w = target ? c->tl[l] : c->dl[l];
+            void* Kc = elem<T>(target ? c->tK : c->dK, (size_t)l * c->kv.layer_stride);
+            void* Vc = elem<T>(target ? c->tV : c->dV, (size_t)l * c->kv.layer_stride);
+            timed(c, DFLASH_K_NORM, R * d * (4 + es), 0, [&] {
+                rmsnorm_rows<T>(L, c->x, c->d, w.attn_norm, rows, c->d, c->cfg.rms_eps, xn, c->d);
+            });
+            timed(c, DFLASH_K_GEMM_QKV, gemm_bytes(c, R, c->qkv_n, d, false), 2 * R * c->qkv_n * d, [&] {
+                gemm<T>(L, xn, c->d, (const T*)w.wqkv, rows, c->qkv_n, c->d, c->qkv, c->qkv_n, false);
+            });
+            QKVStore st;
+            st.qkv = c->qkv;
+            st.ld = c->qkv_n;
+            st.q_off = 0;
+            st.k_off = c->qd;
+            st.v_off = c->qd + c->kvd;
+            st.H = c->H;
+            st.Hkv = c->Hkv;
+            st.hd = c->hd;
+            st.row_seq = row_seq;
+            st.row_pos = row_pos;
+            st.q_norm = w.q_norm;
+            st.k_norm = w.k_norm;
+            st.eps = c->cfg.rms_eps;
+            st.rope = c->rope;
+            st.max_pos = c->max_seq;
+            st.q_out = c->q;
+            st.Kc = Kc;
+            st.Vc = Vc;
+            st.kv = c->kv;
+            st.page_table = c->page_table;
+            st.rows = rows;
+            st.err = c->errw;
+            timed(c, DFLASH_K_ROPE_STORE, R * c->qkv_n * (4 + es), 0, [&] { qk_norm_rope_store<T>(L, st); });
+            AttnParams ap;
+            ap.q = c->q;
+            ap.Kc = Kc;
+            ap.Vc = Vc;
+            ap.kv = c->kv;
+            ap.page_table = c->page_table;
+            ap.row_seq = row_seq;
+            ap.row_pos = row_pos;
+            ap.seq_len = target ? nullptr : c->n;
+            ap.extra = target ? 0 : c->B;
+            ap.rows = rows;
+            ap.group_rows = group_rows;
+            ap.H = c->H;
+            ap.Hkv = c->Hkv;
+            ap.hd = c->hd;
+            ap.max_keys = max_keys;
+            ap.out = c->att;
+            ap.ws = c->attn_ws;
+            ap.ws_bytes = ATTN_WS_BYTES;
+            timed(c, DFLASH_K_ATTENTION, keys_total * 2 * c->kvd * es + 2 * R * c->qd * es,
+                  4.0 * R * c->H * c->hd * (keys_total / std::max(1.0, (double)c->batch)), [&] { attention<T>(L, ap); });
+            timed(c, DFLASH_K_GEMM_O, gemm_bytes(c, R, d, c->qd, true), 2 * R * d * c->qd, [&] {
+                gemm<T>(L, (const T*)c->att, c->qd, (const T*)w.wo, rows, c->d, c->qd, c->x, c->d, true);
+            });
+            timed(c, DFLASH_K_NORM, R * d * (4 + es), 0, [&] {
+                rmsnorm_rows<T>(L, c->x, c->d, w.mlp_norm, rows, c->d, c->cfg.rms_eps, xn, c->d);
+            });
+            timed(c, DFLASH_K_GEMM_GATE_UP, gemm_bytes(c, R, 2.0 * c->F, d, false), 2 * R * 2.0 * c->F * d, [&] {
+                gemm<T>(L, xn, c->d, (const T*)w.wgu, rows, 2 * c->F, c->d, c->gu, 2 * c->F, false);
+            });
+            timed(c, DFLASH_K_SWIGLU, R * c->F * (8 + es), 0, [&] { silu_mul<T>(L, c->gu, c->F, rows, (T*)c->hmid); });
+            timed(c, DFLASH_K_GEMM_DOWN, gemm_bytes(c, R, d, c->F, true), 2 * R * d * c->F, [&] {
+                gemm<T>(L, (const T*)c->hmid, c->F, (const T*)w.wdown, rows, c->d, c->F, c->x, c->d, true);
+            });
+            if (target && capture && c->ctx_slot[l] >= 0)
+                timed(c, DFLASH_K_OTHER, R * d * (4 + es), 0, [&] {
+                    capture_rows<T>(L, c->x, c->d, rows, (T*)c->stage, c->k * c->d, c->ctx_slot[l] * c->d);
+                });
+        }
+    }
+
+    // Context feature rms(W_c stage) and its K/V in every draft layer, stored
+    // at (ctx_seq, ctx_pos); rows with ctx_seq < 0 are skipped.
+    void append_context(int rows, const int* ctx_seq, const int* ctx_pos) {
+        Launch L = c->L();
+        const double R = rows, d = c->d, es = c->esz;
+        timed(c, DFLASH_K_GEMM_FC, gemm_bytes(c, R, d, c->k * d, false), 2 * R * d * c->k * d, [&] {
+            gemm<T>(L, (const T*)c->stage, c->k * c->d, (const T*)c->fc, rows, c->d, c->k * c->d, c->fcout, c->d, false);
+        });
+        timed(c, DFLASH_K_NORM, R * d * (4 + es), 0, [&] {
+            rmsnorm_rows<T>(L, c->fcout, c->d, c->fc_norm, rows, c->d, c->cfg.rms_eps, (T*)c->feat, c->d);
+        });
+        for (int l = 0; l < c->Ld; ++l) {
+            const LayerW& w = c->dl[l];
+            const T* wkv = elem<T>(w.wqkv, (size_t)c->qd * c->d);  // rows wk, wv
+            timed(c, DFLASH_K_GEMM_CTX_KV, gemm_bytes(c, R, 2.0 * c->kvd, d, false), 2 * R * 2.0 * c->kvd * d, [&] {
+                gemm<T>(L, (const T*)c->feat, c->d, wkv, rows, 2 * c->kvd, c->d, c->kvout, 2 * c->kvd, false);
+            });
+            QKVStore st;
+            st.qkv = c->kvout;
+            st.ld = 2 * c->kvd;
+            st.q_off = -1;
+            st.k_off = 0;
+            st.v_off = c->kvd;
+            st.H = c->H;
+            st.Hkv = c->Hkv;
+            st.hd = c->hd;
+            st.row_seq = ctx_seq;
+            st.row_pos = ctx_pos;
+            st.q_norm = nullptr;
+            st.k_norm = w.k_norm;
+            st.eps = c->cfg.rms_eps;
+            st.rope = c->rope;
+            st.max_pos = c->max_seq;
+            st.q_out = nullptr;
+            st.Kc = elem<T>(c->dK, (size_t)l * c->kv.layer_stride);
+            st.Vc = elem<T>(c->dV, (size_t)l * c->kv.layer_stride);
+            st.kv = c->kv;
+            st.page_table = c->page_table;
+            st.rows = rows;
+            st.err = c->errw;
+            timed(c, DFLASH_K_ROPE_STORE, R * 2.0 * c->kvd * (4 + es), 0, [&] { qk_norm_rope_store<T>(L, st); });
+        }
+    }
+
+    // Final norm + shared head + row argmax over `rows` rows of x starting at row0.
+    void head(int row0, int rows, const float* norm, int* out, float* keep) {
+        Launch L = c->L();
+        const double R = rows, d = c->d, es = c->esz, V = c->V;
+        timed(c, DFLASH_K_NORM, R * d * (4 + es), 0, [&] {
+            rmsnorm_rows<T>(L, c->x + (size_t)row0 * c->d, c->d, norm, rows, c->d, c->cfg.rms_eps, (T*)c->xn, c->d);
+        });
+        timed(c, DFLASH_K_GEMM_HEAD, gemm_bytes(c, R, V, d, false), 2 * R * V * d, [&] {
+            gemm<T>(L, (const T*)c->xn, c->d, (const T*)c->head, rows, c->V, c->d, c->logits, c->V, false);
+        });
+        timed(c, DFLASH_K_ARGMAX, R * V * 4, 0, [&] { argmax_rows(L, c->logits, c->V, rows, c->V, out); });
+        if (keep) cudaMemcpyAsync(keep, c->logits, (size_t)rows * c->V * 4, cudaMemcpyDeviceToDevice, c->stream);
+    }
+
+    dflash_status prefill(int batch, const int* lens, const int* toks, int* first) {
+        Launch L = c->L();
+        const int g = c->H / c->Hkv;
+        size_t off = 0;
+        for (int s = 0; s < batch; ++s) {
+            const int P = lens[s];
+            for (int r0 = 0; r0 < P; r0 += PREFILL_CHUNK) {
+                const int rows = std::min(PREFILL_CHUNK, P - r0);
+                CUDA_TRY(c, cudaMemcpyAsync(c->tokens, toks + off + r0, (size_t)rows * 4, cudaMemcpyHostToDevice,
+                                            c->stream));
+                fill_prefill_rows(L, s, r0, rows, c->row_seq, c->row_pos);
+                embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, rows, c->x, c->errw);
+                layers(true, rows, c->row_seq, c->row_pos, 64 / g, r0 + rows, true, (double)(r0 + rows));
+                append_context(rows, c->row_seq, c->row_pos);
+                if (r0 + rows == P)
+                    head(rows - 1, 1, c->final_norm, c->anchor + s,
+                         c->keep_prefill ? c->keep_prefill + (size_t)s * c->V : nullptr);
+            }
+            off += P;
+        }
+        std::vector<int> nh(lens, lens + batch);
+        CUDA_TRY(c, cudaMemcpyAsync(c->n, nh.data(), (size_t)batch * 4, cudaMemcpyHostToDevice, c->stream));
+        CUDA_TRY(c, cudaMemcpyAsync(first, c->anchor, (size_t)batch * 4, cudaMemcpyDeviceToHost, c->stream));
+        return check_device(c);
+    }
+
+    void draft() {
+        Launch L = c->L();
+        const int b = c->batch, B = c->B, g = c->H / c->Hkv;
+        if (c->pending_append) {
+            append_context(b * B, c->ctx_row_seq, c->ctx_row_pos);
+            c->pending_append = false;
+        }
+        if (B == 1) return;
+        timed(c, DFLASH_K_OTHER, (double)b * B * c->d * (4 + c->esz), 0, [&] {
+            block_rows(L, b, B, c->n, c->anchor, nullptr, c->cfg.mask_token, c->V, c->max_seq, c->tokens, c->row_seq,
+                       c->row_pos, c->errw);
+            embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, b * B, c->x, c->errw);
+        });
+        int maxk = 0;
+        double keys = 0;
+        for (int s = 0; s < b; ++s) {
+            maxk = std::max(maxk, c->n_upper[s] + B);
+            keys += c->n_upper[s] + B;
+        }
+        layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), maxk, false, keys);
+        head(0, b * B, c->draft_norm, c->argbuf, c->keep_draft);
+        // drafts[s][j] = argmax of row s*B + 1 + j
+        cudaMemcpy2DAsync(c->drafts, (size_t)(B - 1) * 4, c->argbuf + 1, (size_t)B * 4, (size_t)(B - 1) * 4, b,
+                          cudaMemcpyDeviceToDevice, c->stream);
+    }
+
+    void verify() {
+        Launch L = c->L();
+        const int b = c->batch, B = c->B, g = c->H / c->Hkv;
+        timed(c, DFLASH_K_OTHER, (double)b * B * c->d * (4 + c->esz), 0, [&] {
+            block_rows(L, b, B, c->n, c->anchor, c->proposal, c->cfg.mask_token, c->V, c->max_seq, c->tokens,
+                       c->row_seq, c->row_pos, c->errw);
+            embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, b * B, c->x, c->errw);
+        });
+        int maxk = 0;
+        double keys = 0;
+        for (int s = 0; s < b; ++s) {
+            maxk = std::max(maxk, c->n_upper[s] + B);
+            keys += c->n_upper[s] + B;
+        }
+        layers(true, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), maxk, true, keys);
+        if (c->keep_hidden)
+            cudaMemcpyAsync(c->keep_hidden, c->x, (size_t)b * B * c->d * 4, cudaMemcpyDeviceToDevice, c->stream);
+        head(0, b * B, c->final_norm, c->posterior, c->keep_verify);
+        timed(c, DFLASH_K_OTHER, (double)b * B * 8, 0, [&] {
+            accept(L, b, B, c->proposal, c->posterior, c->n, c->anchor, c->accepted, c->bonus, c->ctx_row_seq,
+                   c->ctx_row_pos);
+        });
+        c->pending_append = true;
+    }
+};
+
+dflash_status capacity_check(dflash_ctx* c) {
+    for (int s = 0; s < c->batch; ++s) {
+        if (c->n_upper[s] + c->B > c->cfg.max_seq_len) {
+            // refresh from the device before refusing
+            std::vector<int> nh(c->batch);
+            CUDA_TRY(c, cudaMemcpyAsync(nh.data(), c->n, (size_t)c->batch * 4, cudaMemcpyDeviceToHost, c->stream));
+            CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+            c->n_upper = nh;
+            if (c->n_upper[s] + c->B > c->cfg.max_seq_len)
+                return c->fail(DFLASH_E_CAPACITY, "sequence %d: length %d + block %d exceeds max_seq_len %d", s,
+                               c->n_upper[s], c->B, c->cfg.max_seq_len);
+        }
+    }
+    return DFLASH_OK;
+}
+
+dflash_status do_draft(dflash_ctx* c) {
+    if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.draft();
+    else Pass<float>{c}.draft();
+    CUDA_TRY(c, cudaGetLastError());
+    return DFLASH_OK;
+}
+
+dflash_status do_verify(dflash_ctx* c) {
+    if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.verify();
+    else Pass<float>{c}.verify();
+    CUDA_TRY(c, cudaGetLastError());
+    for (int s = 0; s < c->batch; ++s) c->n_upper[s] += c->B;
+    return DFLASH_OK;
+}
+
+// Stage user tokens [b, B-1] into ctx->proposal.
+dflash_status load_proposal(dflash_ctx* c, const int32_t* toks) {
+    const size_t n = (size_t)c->batch * (c->B - 1);
+    if (n == 0) return DFLASH_OK;
+    if (toks == c->drafts) {
+        CUDA_TRY(c, cudaMemcpyAsync(c->proposal, toks, n * 4, cudaMemcpyDeviceToDevice, c->stream));
+    } else if (is_device_ptr(toks)) {
+        CUDA_TRY(c, cudaMemcpyAsync(c->proposal, toks, n * 4, cudaMemcpyDeviceToDevice, c->stream));
+    } else {
+        for (size_t i = 0; i < n; ++i)
+            if (toks[i] < 0 || toks[i] >= c->V)
+                return c->fail(DFLASH_E_INVAL, "draft token %zu = %d outside [0, %d)", i, toks[i], c->V);
+        CUDA_TRY(c, cudaMemcpyAsync(c->proposal, toks, n * 4, cudaMemcpyHostToDevice, c->stream));
+    }
+    return DFLASH_OK;
+}
+
+dflash_status store_out(dflash_ctx* c, void* dst, const void* src, size_t bytes, bool* host) {
+    *host = false;
+    if (bytes == 0 || dst == src) return DFLASH_OK;
+    if (is_device_ptr(dst)) {
+        CUDA_TRY(c, cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, c->stream));
+    } else {
+        CUDA_TRY(c, cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, c->stream));
+        *host = true;
+    }
+    return DFLASH_OK;
+}
+
+}  // namespace
+
+// ===================================================================== C ABI
+extern "C" {
+
+dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, void* cuda_stream, dflash_ctx** out) {
+    if (!out) return DFLASH_E_INVAL;
+    *out = nullptr;
+    if (!cfg || !w || !w->target || !w->draft) {
+        g_init_error = "cfg, weights and layer arrays must be non-NULL";
+        return DFLASH_E_INVAL;
+    }
+    std::string why;
+    if (validate(cfg, why) != DFLASH_OK) {
+        g_init_error = why;
+        return DFLASH_E_INVAL;
+    }
+    dflash_ctx* c = new dflash_ctx();
+    c->cfg = *cfg;
+    c->stream = (cudaStream_t)cuda_stream;
+    memset(&c->stats, 0, sizeof c->stats);
+    c->esz = cfg->dtype == DFLASH_DTYPE_BF16 ? 2 : 4;
+    c->d = cfg->d_model;
+    c->H = cfg->n_heads;
+    c->Hkv = cfg->n_kv_heads;
+    c->hd = cfg->head_dim;
+    c->F = cfg->ffn;
+    c->V = cfg->vocab;
+    c->Lt = cfg->target_layers;
+    c->Ld = cfg->draft_layers;
+    c->B = cfg->block_size;
+    c->k = cfg->n_ctx_layers;
+    c->qd = c->H * c->hd;
+    c->kvd = c->Hkv * c->hd;
+    c->qkv_n = c->qd + 2 * c->kvd;
+    c->max_seq = (cfg->max_seq_len + PAGE_TOKENS - 1) / PAGE_TOKENS * PAGE_TOKENS;
+    for (int l = 0; l < 64; ++l) c->ctx_slot[l] = -1;
+    for (int i = 0; i < c->k; ++i) c->ctx_slot[cfg->ctx_layer_ids[i]] = i;
+
+    auto bail = [&](dflash_status s) {
+        g_init_error = c->err;
+        dflash_destroy(c);
+        return s;
+    };
+#define ALLOC(ptr, bytes)                                                                   \
+    do {                                                                                    \
+        (ptr) = (decltype(ptr))dev_alloc(c, (bytes));                                       \
+        if (!(ptr)) {                                                                       \
+            c->fail(DFLASH_E_NOMEM, "device allocation of %zu bytes failed", (size_t)(bytes)); \
+            return bail(DFLASH_E_NOMEM);                                                    \
+        }                                                                                   \
+    } while (0)
+
+    const size_t d = c->d, V = c->V, esz = c->esz;
+    // weights
+    ALLOC(c->embed, V * d * esz);
+    ALLOC(c->head, V * d * esz);
+    ALLOC(c->fc, d * c->k * d * esz);
+    dflash_status s;
+    if ((s = copy_rows(c, c->embed, 0, w->embed, V, d))) return bail(s);
+    if ((s = copy_rows(c, c->head, 0, w->head, V, d))) return bail(s);
+    if ((s = copy_rows(c, c->fc, 0, w->fc, d, c->k * d))) return bail(s);
+    if ((s = copy_norm(c, &c->final_norm, w->final_norm, d, false))) return bail(s);
+    if ((s = copy_norm(c, &c->fc_norm, w->fc_norm, d, false))) return bail(s);
+    if ((s = copy_norm(c, &c->draft_norm, w->draft_norm, d, false))) return bail(s);
+    c->tl.resize(c->Lt);
+    c->dl.resize(c->Ld);
+    for (int l = 0; l < c->Lt; ++l)
+        if ((s = pack_layer(c, w->target[l], c->tl[l], cfg->target_qk_norm != 0))) return bail(s);
+    for (int l = 0; l < c->Ld; ++l)
+        if ((s = pack_layer(c, w->draft[l], c->dl[l], true))) return bail(s);
+
+    // caches: identity page mapping, one run of pages per sequence
+    c->kv.page_tokens = PAGE_TOKENS;
+    c->kv.page_shift = PAGE_SHIFT;
+    c->kv.pages_per_seq = c->max_seq / PAGE_TOKENS;
+    c->kv.n_kv_heads = c->Hkv;
+    c->kv.head_dim = c->hd;
+    const size_t pages = (size_t)cfg->max_batch * c->kv.pages_per_seq;
+    c->kv.layer_stride = (long long)(pages * c->Hkv * PAGE_TOKENS * c->hd);
+    ALLOC(c->tK, (size_t)c->Lt * c->kv.layer_stride * esz);
+    ALLOC(c->tV, (size_t)c->Lt * c->kv.layer_stride * esz);
+    ALLOC(c->dK, (size_t)c->Ld * c->kv.layer_stride * esz);
+    ALLOC(c->dV, (size_t)c->Ld * c->kv.layer_stride * esz);
+    ALLOC(c->page_table, pages * 4);
+    {
+        std::vector<int> pt(pages);
+        for (size_t i = 0; i < pages; ++i) pt[i] = (int)i;
+        if (cudaMemcpyAsync(c->page_table, pt.data(), pages * 4, cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
+            cudaStreamSynchronize(c->stream) != cudaSuccess) {
+            c->fail(DFLASH_E_CUDA, "page table upload failed");
+            return bail(DFLASH_E_CUDA);
+        }
+    }
+    // RoPE table: angle pos * theta^(-2j/hd) in double, stored as fp32 (cos, sin)
+    ALLOC(c->rope, (size_t)c->max_seq * (c->hd / 2) * sizeof(float2));
+    {
+        std::vector<float2> t((size_t)c->max_seq * (c->hd / 2));
+        for (int p = 0; p < c->max_seq; ++p)
+            for (int j = 0; j < c->hd / 2; ++j) {
+                const double inv = pow(cfg->rope_theta, -2.0 * j / c->hd);
+                const double a = (double)p * inv;
+                t[(size_t)p * (c->hd / 2) + j] = make_float2((float)cos(a), (float)sin(a));
+            }
+        if (cudaMemcpy(c->rope, t.data(), t.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
+            c->fail(DFLASH_E_CUDA, "rope table upload failed");
+            return bail(DFLASH_E_CUDA);
+        }
+    }
+    // round buffers
+    const int rb = cfg->max_batch * c->B;
+    c->R = std::max(rb, PREFILL_CHUNK);
+    const size_t R = c->R;
+    ALLOC(c->x, R * d * 4);
+    ALLOC(c->xn, R * d * esz);
+    ALLOC(c->qkv, R * c->qkv_n * 4);
+    ALLOC(c->q, R * c->qd * esz);
+    ALLOC(c->att, R * c->qd * esz);
+    ALLOC(c->gu, R * 2 * c->F * 4);
+    ALLOC(c->hmid, R * c->F * esz);
+    ALLOC(c->stage, R * c->k * d * esz);
+    ALLOC(c->fcout, R * d * 4);
+    ALLOC(c->feat, R * d * esz);
+    ALLOC(c->kvout, R * 2 * c->kvd * 4);
+    ALLOC(c->logits, (size_t)rb * V * 4);
+    ALLOC(c->tokens, R * 4);
+    ALLOC(c->row_seq, R * 4);
+    ALLOC(c->row_pos, R * 4);
+    ALLOC(c->ctx_row_seq, (size_t)rb * 4);
+    ALLOC(c->ctx_row_pos, (size_t)rb * 4);
+    ALLOC(c->n, (size_t)cfg->max_batch * 4);
+    ALLOC(c->anchor, (size_t)cfg->max_batch * 4);
+    ALLOC(c->proposal, (size_t)cfg->max_batch * c->B * 4);
+    ALLOC(c->posterior, (size_t)rb * 4);
+    ALLOC(c->argbuf, (size_t)rb * 4);
+    ALLOC(c->accepted, (size_t)cfg->max_batch * 4);
+    ALLOC(c->bonus, (size_t)cfg->max_batch * 4);
+    ALLOC(c->drafts, (size_t)cfg->max_batch * c->B * 4);
+    ALLOC(c->errw, 16);
+    ALLOC(c->attn_ws, ATTN_WS_BYTES);
+    if (cfg->flags & DFLASH_FLAG_KEEP_LOGITS) {
+        ALLOC(c->keep_prefill, (size_t)cfg->max_batch * V * 4);
+        ALLOC(c->keep_draft, (size_t)rb * V * 4);
+        ALLOC(c->keep_verify, (size_t)rb * V * 4);
+        ALLOC(c->keep_hidden, (size_t)rb * d * 4);
+    }
+    if (cudaMemsetAsync(c->errw, 0, 16, c->stream) != cudaSuccess ||
+        cudaMemsetAsync(c->n, 0, (size_t)cfg->max_batch * 4, c->stream) != cudaSuccess) {
+        c->fail(DFLASH_E_CUDA, "memset failed");
+        return bail(DFLASH_E_CUDA);
+    }
+    for (int i = 0; i < 4; ++i)
+        if (cudaEventCreate(&c->ev[i]) != cudaSuccess) {
+            c->fail(DFLASH_E_CUDA, "event creation failed");
+            return bail(DFLASH_E_CUDA);
+        }
+    c->events = true;
+    memset(c->prof_acc, 0, sizeof c->prof_acc);
+    if ((cfg->flags & DFLASH_FLAG_PROFILE) && dflash_set_profiling(c, 1) != DFLASH_OK) return bail(DFLASH_E_CUDA);
+    if (cudaStreamSynchronize(c->stream) != cudaSuccess) {
+        c->fail(DFLASH_E_CUDA, "weight packing failed: %s", cudaGetErrorString(cudaGetLastError()));
+        return bail(DFLASH_E_CUDA);
+    }
+#undef ALLOC
+    *out = c;
+    return DFLASH_OK;
+}
+
+dflash_status dflash_prefill(dflash_ctx* c, int32_t batch, const int32_t* lens, const int32_t* toks, int32_t* first) {
+    if (!c) return DFLASH_E_INVAL;
+    if (batch < 1 || batch > c->cfg.max_batch) return c->fail(DFLASH_E_INVAL, "batch %d outside [1, %d]", batch, c->cfg.max_batch);
+    if (!lens || !toks || !first) return c->fail(DFLASH_E_INVAL, "NULL argument");
+    size_t total = 0;
+    for (int s = 0; s < batch; ++s) {
+        if (lens[s] < 1) return c->fail(DFLASH_E_INVAL, "prompt %d has length %d", s, lens[s]);
+        if (lens[s] + c->B > c->cfg.max_seq_len)
+            return c->fail(DFLASH_E_CAPACITY, "prompt %d: length %d + block %d exceeds max_seq_len %d", s, lens[s],
+                           c->B, c->cfg.max_seq_len);
+        total += lens[s];
+    }
+    for (size_t i = 0; i < total; ++i)
+        if (toks[i] < 0 || toks[i] >= c->V) return c->fail(DFLASH_E_INVAL, "prompt token %zu = %d outside [0, %d)", i, toks[i], c->V);
+    c->batch = batch;
+    c->state = ST_EMPTY;
+    c->pending_append = false;
+    c->n_upper.assign(lens, lens + batch);
+    if (c->events) cudaEventRecord(c->ev[0], c->stream);
+    dflash_status s = c->cfg.dtype == DFLASH_DTYPE_BF16 ? Pass<bf16>{c}.prefill(batch, lens, toks, first)
+                                                        : Pass<float>{c}.prefill(batch, lens, toks, first);
+    if (s != DFLASH_OK) return s;
+    if (c->events) {
+        cudaEventRecord(c->ev[1], c->stream);
+        cudaEventSynchronize(c->ev[1]);
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, c->ev[0], c->ev[1]);
+        c->stats.prefill_ms += ms;
+    }
+    c->state = ST_READY;
+    return DFLASH_OK;
+}
+
+dflash_status dflash_draft_block(dflash_ctx* c, int32_t* draft_tokens) {
+    if (!c) return DFLASH_E_INVAL;
+    if (c->state != ST_READY) return c->fail(DFLASH_E_STATE, c->state == ST_EMPTY ? "draft_block before prefill" : "draft_block called twice without verify");
+    if (!draft_tokens && c->B > 1) return c->fail(DFLASH_E_INVAL, "draft_tokens is NULL");
+    dflash_status s;
+    if ((s = capacity_check(c))) return s;
+    if ((s = do_draft(c))) return s;
+    bool host = false;
+    if (c->B > 1 && draft_tokens != c->drafts)
+        if ((s = store_out(c, draft_tokens, c->drafts, (size_t)c->batch * (c->B - 1) * 4, &host))) return s;
+    c->state = ST_DRAFTED;
+    if (host) return check_device(c);
+    return DFLASH_OK;
+}
+
+dflash_status dflash_verify(dflash_ctx* c, const int32_t* draft_tokens, int32_t* accepted, int32_t* bonus) {
+    if (!c) return DFLASH_E_INVAL;
+    if (c->state != ST_DRAFTED) return c->fail(DFLASH_E_STATE, "verify without a preceding draft_block");
+    if ((!draft_tokens && c->B > 1) || !accepted || !bonus) return c->fail(DFLASH_E_INVAL, "NULL argument");
+    dflash_status s;
+    if ((s = load_proposal(c, draft_tokens))) return s;
+    if ((s = do_verify(c))) return s;
+    c->state = ST_READY;
+    bool h1 = false, h2 = false;
+    if ((s = store_out(c, accepted, c->accepted, (size_t)c->batch * 4, &h1))) return s;
+    if ((s = store_out(c, bonus, c->bonus, (size_t)c->batch * 4, &h2))) return s;
+    if (h1) {
+        if ((s = check_device(c))) return s;
+        for (int i = 0; i < c->batch; ++i) c->n_upper[i] += accepted[i] + 1 - c->B;  // now exact
+    } else if (h2) {
+        if ((s = check_device(c))) return s;
+    }
+    return DFLASH_OK;
+}
+
+dflash_status dflash_generate(dflash_ctx* c, int32_t batch, const int32_t* lens, const int32_t* toks, int32_t N,
+                              int32_t* out_tokens, int32_t* out_lens, dflash_stats* stats) {
+    if (!c) return DFLASH_E_INVAL;
+    if (N < 1 || !out_tokens || !out_lens) return c->fail(DFLASH_E_INVAL, "max_new_tokens < 1 or NULL output");
+    dflash_status s;
+    std::vector<int> first(batch > 0 ? batch : 1);
+    if ((s = dflash_prefill(c, batch, lens, toks, first.data()))) return s;
+    const int B = c->B;
+    std::vector<int> cnt(batch, 0), acc(batch), bon(batch), dr((size_t)batch * (B > 1 ? B - 1 : 1));
+    for (int i = 0; i < batch; ++i) {
+        out_tokens[(size_t)i * N] = first[i];
+        cnt[i] = 1;
+    }
+    c->stats.tokens += batch;
+    auto done = [&]() {
+        for (int i = 0; i < batch; ++i)
+            if (cnt[i] < N) return false;
+        return true;
+    };
+    while (!done()) {
+        cudaEventRecord(c->ev[0], c->stream);
+        if ((s = dflash_draft_block(c, c->drafts))) return s;
+        cudaEventRecord(c->ev[1], c->stream);
+        if ((s = dflash_verify(c, c->drafts, c->accepted, c->bonus))) return s;
+        cudaEventRecord(c->ev[2], c->stream);
+        CUDA_TRY(c, cudaMemcpyAsync(acc.data(), c->accepted, (size_t)batch * 4, cudaMemcpyDeviceToHost, c->stream));
+        CUDA_TRY(c, cudaMemcpyAsync(bon.data(), c->bonus, (size_t)batch * 4, cudaMemcpyDeviceToHost, c->stream));
+        if (B > 1)
+            CUDA_TRY(c, cudaMemcpyAsync(dr.data(), c->proposal, (size_t)batch * (B - 1) * 4, cudaMemcpyDeviceToHost,
+                                        c->stream));
+        if ((s = check_device(c))) return s;
+        float t1 = 0.f, t2 = 0.f;
+        cudaEventElapsedTime(&t1, c->ev[0], c->ev[1]);
+        cudaEventElapsedTime(&t2, c->ev[1], c->ev[2]);
+        c->stats.draft_ms += t1;
+        c->stats.verify_ms += t2;
+        c->stats.rounds += 1;
+        for (int i = 0; i < batch; ++i) {
+            c->n_upper[i] += acc[i] + 1 - B;
+            c->stats.accepted += acc[i];
+            for (int j = 0; j < acc[i] && cnt[i] < N; ++j) out_tokens[(size_t)i * N + cnt[i]++] = dr[(size_t)i * (B - 1) + j];
+            if (cnt[i] < N) out_tokens[(size_t)i * N + cnt[i]++] = bon[i];
+            c->stats.tokens += acc[i] + 1;
+        }
+        bool room = true;
+        for (int i = 0; i < batch; ++i)
+            if (cnt[i] < N && c->n_upper[i] + B > c->cfg.max_seq_len) room = false;
+        if (!room) return c->fail(DFLASH_E_CAPACITY, "max_seq_len too small for max_new_tokens");
+    }
+    for (int i = 0; i < batch; ++i) out_lens[i] = N;
+    c->stats.kernel_launches = c->launches;
+    if (stats) *stats = c->stats;
+    return DFLASH_OK;
+}
+
+dflash_status dflash_inspect(dflash_ctx* c, int32_t what, int32_t seq, int32_t layer, void* dst, size_t bytes,
+                             size_t* written) {
+    if (!c || !dst) return DFLASH_E_INVAL;
+    size_t need = 0;
+    const void* src = nullptr;
+    const int b = c->batch, B = c->B;
+    auto simple = [&](const void* p, size_t n) -> dflash_status {
+        if (bytes < n) return c->fail(DFLASH_E_INVAL, "buffer of %zu bytes, need %zu", bytes, n);
+        if (!p) return c->fail(DFLASH_E_INVAL, "item not kept (set DFLASH_FLAG_KEEP_LOGITS)");
+        CUDA_TRY(c, cudaMemcpyAsync(dst, p, n, cudaMemcpyDeviceToHost, c->stream));
+        CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+        if (written) *written = n;
+        return DFLASH_OK;
+    };
+    switch (what) {
+        case DFLASH_INSPECT_LENGTHS: return simple(c->n, (size_t)b * 4);
+        case DFLASH_INSPECT_ANCHORS: return simple(c->anchor, (size_t)b * 4);
+        case DFLASH_INSPECT_POSTERIOR: return simple(c->posterior, (size_t)b * B * 4);
+        case DFLASH_INSPECT_LOGITS_PREFILL: return simple(c->keep_prefill, (size_t)b * c->V * 4);
+        case DFLASH_INSPECT_LOGITS_DRAFT: return simple(c->keep_draft, (size_t)b * B * c->V * 4);
+        case DFLASH_INSPECT_LOGITS_VERIFY: return simple(c->keep_verify, (size_t)b * B * c->V * 4);
+        case DFLASH_INSPECT_HIDDEN_VERIFY: return simple(c->keep_hidden, (size_t)b * B * c->d * 4);
+        case DFLASH_INSPECT_PROFILE: {
+            if (bytes < sizeof(c->prof_acc)) return c->fail(DFLASH_E_INVAL, "buffer too small");
+            dflash_status s = prof_drain(c);
+            if (s) return s;
+            memcpy(dst, c->prof_acc, sizeof(c->prof_acc));
+            if (written) *written = sizeof(c->prof_acc);
+            return DFLASH_OK;
+        }
+        case DFLASH_INSPECT_PROFILE_RESET: {
+            dflash_status s = prof_drain(c);
+            if (s) return s;
+            memset(c->prof_acc, 0, sizeof(c->prof_acc));
+            if (written) *written = 0;
+            return DFLASH_OK;
+        }
+        case DFLASH_INSPECT_STATS: {
+            if (bytes < sizeof(dflash_stats)) return c->fail(DFLASH_E_INVAL, "buffer too small");
+            c->stats.kernel_launches = c->launches;
+            memcpy(dst, &c->stats, sizeof(dflash_stats));
+            if (written) *written = sizeof(dflash_stats);
+            return DFLASH_OK;
+        }
+        case DFLASH_INSPECT_TARGET_K:
+        case DFLASH_INSPECT_TARGET_V:
+        case DFLASH_INSPECT_DRAFT_K:
+        case DFLASH_INSPECT_DRAFT_V: {
+            const bool tgt = what == DFLASH_INSPECT_TARGET_K || what == DFLASH_INSPECT_TARGET_V;
+            const int nl = tgt ? c->Lt : c->Ld;
+            if (seq < 0 || seq >= b || layer < 0 || layer >= nl) return c->fail(DFLASH_E_INVAL, "seq/layer out of range");
+            int ns = 0;
+            CUDA_TRY(c, cudaMemcpyAsync(&ns, c->n + seq, 4, cudaMemcpyDeviceToHost, c->stream));
+            CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+            need = (size_t)ns * c->kvd * c->esz;
+            if (bytes < need) return c->fail(DFLASH_E_INVAL, "buffer of %zu bytes, need %zu", bytes, need);
+            void* base = (what == DFLASH_INSPECT_TARGET_K) ? c->tK : (what == DFLASH_INSPECT_TARGET_V) ? c->tV
+                       : (what == DFLASH_INSPECT_DRAFT_K) ? c->dK : c->dV;
+            std::vector<int> pt(c->kv.pages_per_seq);
+            CUDA_TRY(c, cudaMemcpy(pt.data(), c->page_table + (size_t)seq * c->kv.pages_per_seq, pt.size() * 4,
+                                   cudaMemcpyDeviceToHost));
+            const size_t page_elems = (size_t)c->Hkv * PAGE_TOKENS * c->hd;
+            std::vector<char> page(page_elems * c->esz);
+            char* o = (char*)dst;
+            for (int p0 = 0; p0 < ns; p0 += PAGE_TOKENS) {
+                const char* src_page = (const char*)base +
+                    ((size_t)layer * c->kv.layer_stride + (size_t)pt[p0 / PAGE_TOKENS] * page_elems) * c->esz;
+                CUDA_TRY(c, cudaMemcpy(page.data(), src_page, page.size(), cudaMemcpyDeviceToHost));
+                for (int t = p0; t < std::min(ns, p0 + PAGE_TOKENS); ++t)
+                    for (int h = 0; h < c->Hkv; ++h)
+                        memcpy(o + ((size_t)t * c->Hkv + h) * c->hd * c->esz,
+                               page.data() + (((size_t)h * PAGE_TOKENS) + (t - p0)) * c->hd * c->esz, c->hd * c->esz);
+            }
+            if (written) *written = need;
+            return DFLASH_OK;
+        }
+        default: return c->fail(DFLASH_E_INVAL, "unknown inspect item %d", what);
+    }
+    (void)src;
+}
+
+dflash_status dflash_set_profiling(dflash_ctx* c, int32_t on) {
+    if (!c) return DFLASH_E_INVAL;
+    if (on && c->prof_ev.empty()) {
+        c->prof_ev.resize(4096);
+        for (auto& e : c->prof_ev) CUDA_TRY(c, cudaEventCreate(&e));
+    }
+    if (!on) {
+        dflash_status s = prof_drain(c);
+        if (s) return s;
+    }
+    c->profiling = on != 0;
+    return DFLASH_OK;
+}
+
+void dflash_destroy(dflash_ctx* c) {
+    if (!c) return;
+    if (c->stream) cudaStreamSynchronize(c->stream);
+    else cudaDeviceSynchronize();
+    for (void* p : c->allocs) {
+        if (c->cfg.free) c->cfg.free(p, c->cfg.alloc_user);
+        else cudaFree(p);
+    }
+    if (c->events)
+        for (int i = 0; i < 4; ++i) cudaEventDestroy(c->ev[i]);
+    for (auto& e : c->prof_ev) cudaEventDestroy(e);
+    delete c;
+}
+
+const char* dflash_last_error(const dflash_ctx* c) {
+    return c ? c->err.c_str() : g_init_error.c_str();
+}
+
+}  // extern "C"

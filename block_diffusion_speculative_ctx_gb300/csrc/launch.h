@@ -1,0 +1,110 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Each launcher enqueues its kernel(s) on ctx.stream and
+// bumps ctx.launches once per kernel launched.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dfl {
+
+struct Launch {
+    cudaStream_t stream;
+    long long* launches;  // incremented once per kernel launch
+    void bump(int n = 1) const {
+        if (launches) *launches += n;
+    }
+};
+
+// ---- GEMM: C[M, N] (fp32, row stride ldc) = or += A[M, K] (T, stride lda) . W[N, K]^T.
+// K, lda and the W row length are multiples of 8; A and W are 16-byte aligned.
+template <typename T>
+void gemm(const Launch& L, const T* A, int lda, const T* W, int M, int N, int K, float* C, int ldc, bool accumulate);
+
+// ---- row kernels
+template <typename T>
+void embed_rows(const Launch& L, const int* tokens, const T* embed, int vocab, int d, int rows, float* x,
+                uint32_t* err);
+template <typename T>
+void rmsnorm_rows(const Launch& L, const float* x, int ldx, const float* w, int rows, int d, float eps, T* out,
+                  int ldo);
+// Per-row RMSNorm of rows gathered by index (row_idx[i] -> x row), used for the
+// last prompt row of each sequence before the head.
+template <typename T>
+void rmsnorm_gather(const Launch& L, const float* x, int ldx, const int* row_idx, const float* w, int rows, int d,
+                    float eps, T* out, int ldo);
+
+struct QKVStore {
+    const float* qkv;     // [rows, ld] fp32 GEMM output
+    int ld;
+    int q_off, k_off, v_off;  // column offsets; q_off < 0: no query heads in this pass
+    int H, Hkv, hd;
+    const int* row_seq;   // [rows]; < 0 = padding row (skipped)
+    const int* row_pos;   // [rows]
+    const float* q_norm;  // [hd] or nullptr
+    const float* k_norm;  // [hd] or nullptr
+    float eps;
+    const float2* rope;   // [max_pos][hd/2] (cos, sin)
+    int max_pos;
+    void* q_out;          // T [rows, H*hd] or nullptr
+    void* Kc;             // cache layer base (T)
+    void* Vc;
+    KVLayout kv;
+    const int* page_table;
+    int rows;
+    uint32_t* err;
+};
+template <typename T>
+void qk_norm_rope_store(const Launch& L, const QKVStore& p);
+
+template <typename T>
+void silu_mul(const Launch& L, const float* gu, int F, int rows, T* out);
+
+// Copy fp32 residual rows into a bf16/fp32 staging buffer at column offset col
+// (context-layer capture): stage[r * ld_stage + col + c] = x[r * d + c].
+template <typename T>
+void capture_rows(const Launch& L, const float* x, int d, int rows, T* stage, int ld_stage, int col);
+
+// Row argmax over logits [rows, V] (row stride ld); lowest index wins on ties.
+void argmax_rows(const Launch& L, const float* logits, long long ld, int rows, int V, int* out);
+
+// ---- attention
+struct AttnParams {
+    const void* q;        // T [rows, H*hd]
+    const void* Kc;       // cache layer base
+    const void* Vc;
+    KVLayout kv;
+    const int* page_table;
+    const int* row_seq;   // [rows]
+    const int* row_pos;   // [rows]
+    const int* seq_len;   // non-causal: keys [0, seq_len[s] + extra); causal: nullptr, keys [0, pos]
+    int extra;
+    int rows;
+    int group_rows;       // rows per query group (all from one sequence)
+    int H, Hkv, hd;
+    int max_keys;         // host upper bound on keys seen by any row
+    void* out;            // T [rows, H*hd]
+    float* ws;            // split workspace (fp32)
+    size_t ws_bytes;
+};
+template <typename T>
+void attention(const Launch& L, const AttnParams& p);
+
+// ---- round bookkeeping
+// Block rows of a draft (proposal == nullptr) or verify pass: token of row
+// s*B+j is anchor[s] (j == 0), the mask id (draft) or proposal[s*(B-1)+j-1]
+// (verify); position n[s]+j.
+void block_rows(const Launch& L, int batch, int B, const int* n, const int* anchor, const int* proposal,
+                int mask, int vocab, int max_pos, int* tokens, int* row_seq, int* row_pos, uint32_t* err);
+
+// Greedy acceptance ([review] §4.1): a_s, bonus_s, n_s += a_s + 1, anchor_s = bonus_s,
+// and the context rows to append next (row s*B+j for j <= a_s at position n_old+j).
+void accept(const Launch& L, int batch, int B, const int* proposal, const int* posterior, int* n, int* anchor,
+            int* accepted, int* bonus, int* ctx_row_seq, int* ctx_row_pos);
+
+// Gather int32 from a device array by index (used to read the last prompt row's argmax).
+void fill_prefill_rows(const Launch& L, int seq, int start_pos, int rows, int* row_seq, int* row_pos);
+
+}  // namespace dfl

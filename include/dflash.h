@@ -1,0 +1,268 @@
+/*
+ * dflash.h - C ABI of the GB300 (sm_103a) greedy block-diffusion speculative
+ * decoding round: target prefill, block drafting with target-context KV
+ * injection, one-pass target verification, greedy acceptance and rollback.
+ *
+ * The operations follow two public pages:
+ *   [digest] "DFlash: Block Diffusion for Flash Speculative Decoding"
+ *            (paper digest: Method / Inference §4.1, the greedy decoding-round
+ *            and draft-layer pseudocode, "Paper vs code").
+ *   [review] "DFlash: Why a Diffusion Drafter Can Accelerate an Autoregressive
+ *            Model" (technical review: §2.3 eq. 2, §4.1, Algorithm 1,
+ *            §5.1 eq. 9-10).
+ *
+ * Conventions
+ * -----------
+ * - Matrices are row-major [out_features, in_features] (y = W x), element
+ *   type given by dflash_config.dtype (fp32 or bf16).  Norm scales are fp32.
+ * - Every call is ordered on the CUDA stream given to dflash_init.  A call
+ *   whose outputs are host pointers returns after the results are on the host;
+ *   a call whose outputs are device pointers returns without synchronising.
+ * - Token arrays may be host or device memory; the library asks the CUDA
+ *   runtime which one a pointer is.
+ * - No call throws, aborts or traps.  Each returns a dflash_status; the text
+ *   of the last failure is available from dflash_last_error.  A call that
+ *   fails a precondition changes no state.
+ * - Device-side checks (for example a token id outside [0, vocab) passed in
+ *   device memory) never fault: they record an error word that the next
+ *   synchronising call turns into DFLASH_E_DEVICE_CHECK.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DFLASH_OK = 0,
+    DFLASH_E_INVAL = 1,        /* bad argument or inconsistent configuration */
+    DFLASH_E_NOMEM = 2,        /* a device allocation failed */
+    DFLASH_E_CUDA = 3,         /* a CUDA runtime call failed */
+    DFLASH_E_STATE = 4,        /* call out of order (verify before draft, draft before prefill, ...) */
+    DFLASH_E_CAPACITY = 5,     /* a sequence would grow past max_seq_len */
+    DFLASH_E_TIMEOUT = 6,      /* a bounded device-side wait ran out */
+    DFLASH_E_DEVICE_CHECK = 7  /* a device-side argument check failed */
+} dflash_status;
+
+enum { DFLASH_DTYPE_F32 = 0, DFLASH_DTYPE_BF16 = 1 };
+
+/* Flags (dflash_config.flags). */
+enum {
+    DFLASH_FLAG_KEEP_LOGITS = 1, /* keep fp32 logits of the last prefill / draft / verify for dflash_inspect */
+    DFLASH_FLAG_PROFILE = 2      /* time every kernel class with CUDA events (see DFLASH_INSPECT_PROFILE) */
+};
+
+/* Kernel classes reported by DFLASH_INSPECT_PROFILE. */
+enum {
+    DFLASH_K_GEMM_QKV = 0,     /* fused q/k/v projection (target and draft layers) */
+    DFLASH_K_GEMM_O = 1,       /* attention output projection + residual */
+    DFLASH_K_GEMM_GATE_UP = 2, /* SwiGLU gate/up projection */
+    DFLASH_K_GEMM_DOWN = 3,    /* SwiGLU down projection + residual */
+    DFLASH_K_GEMM_HEAD = 4,    /* shared LM head */
+    DFLASH_K_GEMM_FC = 5,      /* context fusion W_c */
+    DFLASH_K_GEMM_CTX_KV = 6,  /* context key/value projection of the draft layers */
+    DFLASH_K_ATTENTION = 7,
+    DFLASH_K_NORM = 8,
+    DFLASH_K_ROPE_STORE = 9,
+    DFLASH_K_SWIGLU = 10,
+    DFLASH_K_ARGMAX = 11,
+    DFLASH_K_OTHER = 12,
+    DFLASH_K_COUNT = 13
+};
+
+/* One kernel class in the profile: launches, summed device time (CUDA events
+ * bracketing each launch on the session stream), and the algorithmic bytes
+ * moved and flops performed by those launches. */
+typedef struct {
+    int64_t launches;
+    double ms;
+    double bytes;
+    double flops;
+} dflash_profile_entry;
+
+enum { DFLASH_MAX_CTX_LAYERS = 16 };
+
+/* Device allocator used for every library-owned buffer.  Returns NULL on
+ * failure.  When both are NULL the library uses cudaMalloc / cudaFree. */
+typedef void* (*dflash_alloc_fn)(size_t bytes, void* user);
+typedef void (*dflash_free_fn)(void* ptr, void* user);
+
+typedef struct {
+    int32_t dtype;             /* DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16 */
+    int32_t vocab;             /* V */
+    int32_t d_model;           /* d; multiple of 64 */
+    int32_t n_heads;           /* H query heads */
+    int32_t n_kv_heads;        /* H_kv; H % H_kv == 0 */
+    int32_t head_dim;          /* 64 or 128 */
+    int32_t ffn;               /* SwiGLU hidden size F; multiple of 64 */
+    int32_t target_layers;     /* L_t */
+    int32_t target_qk_norm;    /* 1: per-head RMSNorm of q and k in target layers */
+    int32_t draft_layers;      /* L_d (the drafter always normalises q and k per head) */
+    int32_t block_size;        /* B: anchor + B-1 mask positions; 1 <= B <= 32 */
+    int32_t n_ctx_layers;      /* k target layers whose hidden states form the context feature */
+    int32_t ctx_layer_ids[DFLASH_MAX_CTX_LAYERS]; /* 0-based target layers, residual after the layer */
+    int32_t mask_token;        /* id embedded at the B-1 mask positions */
+    int32_t max_batch;         /* sequences per session */
+    int32_t max_seq_len;       /* capacity per sequence: prompt + generated + B */
+    int32_t flags;             /* DFLASH_FLAG_* */
+    float rms_eps;             /* RMSNorm epsilon */
+    double rope_theta;         /* RoPE base */
+    dflash_alloc_fn alloc;     /* optional allocator (see above) */
+    dflash_free_fn free;
+    void* alloc_user;
+} dflash_config;
+
+/* One decoder layer.  Device pointers; read only inside dflash_init (the
+ * library copies them into its own layout), so they may be freed afterwards. */
+typedef struct {
+    const void* wq;            /* [H*hd, d] */
+    const void* wk;            /* [H_kv*hd, d] */
+    const void* wv;            /* [H_kv*hd, d] */
+    const void* wo;            /* [d, H*hd] */
+    const void* w_gate;        /* [F, d] */
+    const void* w_up;          /* [F, d] */
+    const void* w_down;        /* [d, F] */
+    const float* attn_norm;    /* [d] */
+    const float* mlp_norm;     /* [d] */
+    const float* q_norm;       /* [hd]; NULL for target layers without QK-norm */
+    const float* k_norm;       /* [hd]; NULL for target layers without QK-norm */
+} dflash_layer_weights;
+
+/* Target decoder plus drafter.  The drafter shares the target's embedding
+ * table and LM head ([digest] Method, Training §4.2 step 6; Paper vs code
+ * "Embedding and head"). */
+typedef struct {
+    const void* embed;                     /* [V, d] */
+    const void* head;                      /* [V, d] */
+    const float* final_norm;               /* [d] */
+    const dflash_layer_weights* target;    /* host array of target_layers entries */
+    const void* fc;                        /* W_c [d, k*d] (context fusion, [review] §5.1 eq. 9) */
+    const float* fc_norm;                  /* [d] */
+    const dflash_layer_weights* draft;     /* host array of draft_layers entries */
+    const float* draft_norm;               /* [d] drafter's final RMSNorm */
+} dflash_weights;
+
+typedef struct {
+    int64_t rounds;            /* draft+verify rounds run by dflash_generate */
+    int64_t tokens;            /* tokens emitted, first tokens included */
+    int64_t accepted;          /* accepted drafts, summed over sequences and rounds */
+    double prefill_ms;         /* device time, CUDA events on the session stream */
+    double draft_ms;           /* summed over rounds */
+    double verify_ms;          /* summed over rounds */
+    int64_t kernel_launches;   /* kernels this session has launched */
+} dflash_stats;
+
+typedef struct dflash_ctx dflash_ctx; /* opaque; owned by the library */
+
+/* Create a session: validate cfg, allocate the paged target KV cache, the
+ * draft context cache and all round buffers for max_batch x max_seq_len
+ * (nothing is allocated later), and pack the weights into the library's
+ * layout.  cuda_stream is a cudaStream_t (NULL = legacy default stream).
+ * Errors: E_INVAL (cfg), E_NOMEM, E_CUDA.  *out is NULL on failure. */
+dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, void* cuda_stream,
+                          dflash_ctx** out);
+
+/* Target prefill of a new batch ([digest] greedy decoding-round pseudocode,
+ * prefill and fuse steps; [review] §5.1): a causal forward over each prompt,
+ * the first token = argmax of the last row, and the context feature
+ * RMSNorm(W_c [h_l1; ...; h_lk]) of every prompt position injected as keys and
+ * values into every draft layer.  Afterwards each sequence's committed length
+ * n_i = prompt_lens[i] and its anchor is its first token.
+ * prompt_lens: host [batch]; prompt_tokens: host, concatenated (sum of lens);
+ * first_tokens: host [batch] output.
+ * Errors: E_INVAL (batch outside [1, max_batch], a length < 1, a token outside
+ * [0, V)), E_CAPACITY (length + block_size > max_seq_len), E_CUDA. */
+dflash_status dflash_prefill(dflash_ctx* ctx, int32_t batch, const int32_t* prompt_lens,
+                             const int32_t* prompt_tokens, int32_t* first_tokens);
+
+/* One drafting pass ([digest] Inference steps 2-3 and the draft-layer
+ * pseudocode; [review] §5.1 eq. 10).  First appends the context features of
+ * the anchor and accepted drafts of the previous verify (a_i + 1 rows per
+ * sequence), then runs the drafter once over [anchor, MASK x (B-1)] at
+ * positions n_i .. n_i+B-1, with bidirectional attention over
+ * [context K/V ; block K/V], and writes the argmax of the shared head on the
+ * B-1 mask rows.  The stored context entries are not modified.
+ * draft_tokens: [batch, B-1] int32, host or device.
+ * Errors: E_STATE (no prefill, or a draft not yet verified), E_CAPACITY, E_CUDA. */
+dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t* draft_tokens);
+
+/* Verify a proposal with one causal target pass over [anchor, d_1..d_{B-1}]
+ * at positions n_i .. n_i+B-1 ([digest] Inference step 4; [review] §4.1,
+ * Algorithm 1).  Accepts the longest prefix with d_j equal to the target's
+ * argmax at the position before it (a_i drafts), sets bonus_i to the target's
+ * argmax after that prefix, keeps target cache entries for the anchor and the
+ * a_i accepted drafts only (n_i += a_i + 1), and makes bonus_i the next
+ * anchor.  The proposal need not come from dflash_draft_block: any tokens in
+ * [0, V) are verified exactly.
+ * draft_tokens: [batch, B-1] int32 input; accepted, bonus: [batch] int32
+ * outputs; each host or device.
+ * Errors: E_STATE (no dflash_draft_block since the last verify), E_INVAL
+ * (host token outside [0, V)), E_DEVICE_CHECK (device token outside [0, V),
+ * reported at the next synchronising call), E_CUDA. */
+dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* draft_tokens, int32_t* accepted,
+                            int32_t* bonus);
+
+/* Greedy speculative generation ([digest] greedy decoding-round pseudocode):
+ * prefill, then rounds of draft_block + verify until every sequence has
+ * max_new_tokens tokens (the first token counts); each sequence's output is
+ * cut to max_new_tokens.  out_tokens: host [batch, max_new_tokens];
+ * out_lens: host [batch] (always max_new_tokens); stats may be NULL. */
+dflash_status dflash_generate(dflash_ctx* ctx, int32_t batch, const int32_t* prompt_lens,
+                              const int32_t* prompt_tokens, int32_t max_new_tokens, int32_t* out_tokens,
+                              int32_t* out_lens, dflash_stats* stats);
+
+/* Inspection of session state (for tests and profiling).  Copies into host
+ * memory; synchronises the stream.  *written receives the byte count.
+ *   DFLASH_INSPECT_LENGTHS        int32 [batch]: committed length n_i
+ *   DFLASH_INSPECT_ANCHORS        int32 [batch]
+ *   DFLASH_INSPECT_POSTERIOR      int32 [batch, B]: target argmax of the last verify
+ *   DFLASH_INSPECT_TARGET_K/V     dtype [n_seq, H_kv, hd] of (seq, layer), n_seq committed rows
+ *   DFLASH_INSPECT_DRAFT_K/V      same for the draft context cache
+ *   DFLASH_INSPECT_LOGITS_PREFILL fp32 [batch, V]   (needs DFLASH_FLAG_KEEP_LOGITS)
+ *   DFLASH_INSPECT_LOGITS_DRAFT   fp32 [batch, B, V] (all B rows of the last draft)
+ *   DFLASH_INSPECT_LOGITS_VERIFY  fp32 [batch, B, V]
+ *   DFLASH_INSPECT_STATS          dflash_stats
+ *   DFLASH_INSPECT_HIDDEN_VERIFY  fp32 [batch, B, d]: final residual of the last verify
+ *   DFLASH_INSPECT_PROFILE        dflash_profile_entry [DFLASH_K_COUNT] accumulated since the last reset
+ * Errors: E_INVAL (unknown item, seq/layer out of range, bytes too small). */
+enum {
+    DFLASH_INSPECT_LENGTHS = 1,
+    DFLASH_INSPECT_ANCHORS = 2,
+    DFLASH_INSPECT_POSTERIOR = 3,
+    DFLASH_INSPECT_TARGET_K = 4,
+    DFLASH_INSPECT_TARGET_V = 5,
+    DFLASH_INSPECT_DRAFT_K = 6,
+    DFLASH_INSPECT_DRAFT_V = 7,
+    DFLASH_INSPECT_LOGITS_PREFILL = 8,
+    DFLASH_INSPECT_LOGITS_DRAFT = 9,
+    DFLASH_INSPECT_LOGITS_VERIFY = 10,
+    DFLASH_INSPECT_STATS = 11,
+    DFLASH_INSPECT_HIDDEN_VERIFY = 12,
+    DFLASH_INSPECT_PROFILE = 13,       /* dflash_profile_entry [DFLASH_K_COUNT]; needs DFLASH_FLAG_PROFILE */
+    DFLASH_INSPECT_PROFILE_RESET = 14  /* clears the profile; copies nothing */
+};
+dflash_status dflash_inspect(dflash_ctx* ctx, int32_t what, int32_t seq, int32_t layer, void* host_dst,
+                             size_t bytes, size_t* written);
+
+/* Turn kernel-class timing on (1) or off (0) for this session.  While on,
+ * every kernel class launch is bracketed by CUDA events on the session stream
+ * and its algorithmic bytes and flops are recorded; read the totals with
+ * DFLASH_INSPECT_PROFILE.  Timing adds event records between launches, so
+ * headline timings are taken with it off.  Errors: E_INVAL (ctx NULL), E_CUDA. */
+dflash_status dflash_set_profiling(dflash_ctx* ctx, int32_t on);
+
+/* Release every library-owned buffer.  NULL is a no-op. */
+void dflash_destroy(dflash_ctx* ctx);
+
+/* Text of the last failure on ctx (or of the last failed dflash_init when ctx
+ * is NULL).  Valid until the next call on the same ctx. */
+const char* dflash_last_error(const dflash_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

@@ -1,0 +1,279 @@
+"""GPU path (through the C ABI) against the fp64 CPU oracle on the same seeded
+inputs.
+
+fp32 workloads: tokens, acceptance lengths and committed lengths bit-exact;
+logits within max-abs 1e-3.  bf16 workloads: logits within max-abs 5e-2,
+final hidden states within rel-L2 1e-2, tokens identical except where the
+oracle's top-2 logit margin is below 5e-2 (after such a position the two
+streams may diverge, so the comparison stops there).  The oracle never sees
+a GPU result: proposals are built from the oracle's own greedy stream and fed
+to both sides.
+"""
+import numpy as np
+import pytest
+
+import synth
+from synth import configs
+from oracle import model as om, spec
+
+pytestmark = pytest.mark.gpu
+
+F32_LOGIT_TOL = 1e-3
+BF16_LOGIT_TOL = 5e-2
+BF16_HIDDEN_REL = 1e-2
+BF16_MARGIN = 5e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from block_diffusion_speculative_ctx_gb300 import build
+    build.build()
+
+
+def _session(w, **kw):
+    from block_diffusion_speculative_ctx_gb300 import Session
+    return Session(w, **kw)
+
+
+def _tokens_match(gpu_tok, ora_logits, bf16):
+    """Compare argmax tokens; in bf16 return the first index where a mismatch
+    sits at a near-tie (-1 if none).  A mismatch at a clear margin fails."""
+    ora_tok = np.argmax(ora_logits, axis=-1)
+    if not bf16:
+        np.testing.assert_array_equal(gpu_tok, ora_tok)
+        return -1
+    margin = spec.top2_margin(ora_logits)
+    bad = np.nonzero(gpu_tok != ora_tok)[0]
+    for i in bad:
+        assert margin[i] < BF16_MARGIN, f"token {i}: gpu {gpu_tok[i]} oracle {ora_tok[i]} margin {margin[i]}"
+    return int(bad[0]) if len(bad) else -1
+
+
+def _rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), **wkw):
+    w = configs.get(name)
+    if wkw:
+        w = w.with_(**wkw)
+    bf16 = w.dtype == "bf16"
+    ltol = BF16_LOGIT_TOL if bf16 else F32_LOGIT_TOL
+    m = om.Model(w)
+    prompts = synth.prompts(w)
+    n_ar = 1 + rounds * w.block_size + 1
+    streams = [spec.ar_generate(m, p, n_ar)[0] for p in prompts]
+    props = [spec.planted_proposer(s, taus, w.vocab) for s in streams]
+    states = [spec.prefill(m, p) for p in prompts]
+    sess = _session(w, keep_logits=True, max_seq_len=max(w.prompt_lens) + (rounds + 2) * w.block_size + 8)
+    try:
+        first = sess.prefill(prompts)
+        plog = sess.logits("prefill")
+        for s, st in enumerate(states):
+            assert np.abs(plog[s] - st.first_logits).max() <= ltol
+        if _tokens_match(first, np.stack([st.first_logits for st in states]), bf16) >= 0:
+            return 0
+        # context K/V after prefill
+        for s, st in enumerate(states):
+            for l in range(w.draft_layers):
+                k = sess.cache("draft", "k", s, l)
+                assert k.shape == st.dcache.k[l].shape
+                assert _rel_l2(k, st.dcache.k[l]) < (2e-2 if bf16 else 1e-5)
+        compared = 0
+        for r in range(rounds):
+            drafts = sess.draft_block()
+            dlog = sess.logits("draft") if w.block_size > 1 else None   # block 1 runs no drafter
+            diverged = False
+            proposals = []
+            for s, st in enumerate(states):
+                od, odl = spec.draft(m, st)
+                if dlog is not None:
+                    assert np.abs(dlog[s] - odl).max() <= ltol, f"round {r} seq {s} draft logits"
+                if w.block_size > 1 and _tokens_match(drafts[s], odl[1:], bf16) >= 0:
+                    diverged = True
+                proposals.append(props[s](st, od))
+            prop = np.stack(proposals).astype(np.int32) if w.block_size > 1 else np.zeros((len(states), 1), np.int32)
+            acc, bon = sess.verify(prop)
+            vlog = sess.logits("verify")
+            hid = sess.hidden_verify()
+            post = sess.posterior()
+            lens = sess.lengths()
+            for s, st in enumerate(states):
+                n0 = st.committed
+                rd = spec.verify(m, st, prop[s][: w.block_size - 1], keep_logits=True)
+                assert np.abs(vlog[s] - rd.verify_logits).max() <= ltol, f"round {r} seq {s} verify logits"
+                if _tokens_match(post[s], rd.verify_logits, bf16) >= 0:
+                    diverged = True
+                    continue
+                assert acc[s] == rd.accepted and bon[s] == rd.bonus
+                assert lens[s] == st.committed == n0 + rd.accepted + 1
+            compared += 1
+            if diverged:
+                break
+        if compared == rounds:
+            for s, st in enumerate(states):
+                for l in (0, w.target_layers - 1):
+                    k = sess.cache("target", "k", s, l)
+                    v = sess.cache("target", "v", s, l)
+                    assert k.shape == st.tcache.k[l].shape
+                    assert _rel_l2(k, st.tcache.k[l]) < (2e-2 if bf16 else 1e-5)
+                    assert _rel_l2(v, st.tcache.v[l]) < (2e-2 if bf16 else 1e-5)
+        return compared
+    finally:
+        sess.close()
+
+
+def test_tiny_f32_stepwise():
+    assert run_stepwise("tiny_f32") == 6
+
+
+def test_tiny_f32_ragged_batch_stepwise():
+    assert run_stepwise("tiny_f32_b3") == 6
+
+
+def test_small_f32_hd128_block16_stepwise():
+    assert run_stepwise("small_f32", rounds=4) == 4
+
+
+def test_small_bf16_stepwise():
+    assert run_stepwise("small_bf16", rounds=4) >= 2
+
+
+def test_small_bf16_llama_batch4_stepwise():
+    assert run_stepwise("small_bf16_llama", rounds=4) >= 2
+
+
+def test_block_size_one_is_plain_greedy():
+    assert run_stepwise("tiny_f32_b3", rounds=5, block_size=1) == 5
+
+
+def test_tiny_f32_generate_equals_oracle_greedy():
+    """The full loop through dflash_generate reproduces the oracle's plain
+    greedy decode token for token (losslessness on the GPU path)."""
+    w = configs.get("tiny_f32")
+    m = om.Model(w)
+    p = synth.prompts(w)[0]
+    ar, _ = spec.ar_generate(m, p, w.max_new_tokens)
+    sess = _session(w)
+    try:
+        out, st = sess.generate([p], w.max_new_tokens)
+        np.testing.assert_array_equal(out[0], ar)
+        assert st.tokens >= w.max_new_tokens and st.rounds >= 1
+        assert st.kernel_launches > 0
+    finally:
+        sess.close()
+
+
+def test_ragged_generate_equals_oracle_greedy():
+    w = configs.get("tiny_f32_b3")
+    m = om.Model(w)
+    ps = synth.prompts(w)
+    sess = _session(w)
+    try:
+        out, st = sess.generate(ps, w.max_new_tokens)
+        for s, p in enumerate(ps):
+            ar, _ = spec.ar_generate(m, p, w.max_new_tokens)
+            np.testing.assert_array_equal(out[s], ar)
+    finally:
+        sess.close()
+
+
+def test_bf16_hidden_rel_l2_against_pure_fp64():
+    """Final residual and logits of a verify block against the oracle without
+    any bf16 rounding of activations (plain fp64 on the bf16 weights).  The
+    proposal is a fixed synthetic token block, the same on both sides."""
+    w = configs.get("small_bf16")
+    m = om.Model(w, act_round=False)
+    prompts = synth.prompts(w)
+    proposal = synth.uniform_ints(123, 0x51, len(prompts) * (w.block_size - 1), w.vocab).reshape(len(prompts), -1)
+    sess = _session(w, keep_logits=True)
+    try:
+        first = sess.prefill(prompts)
+        sess.draft_block()
+        sess.verify(proposal.astype(np.int32))
+        hid = sess.hidden_verify()
+        vlog = sess.logits("verify")
+        checked = 0
+        for s, p in enumerate(prompts):
+            st = spec.prefill(m, p)
+            if first[s] != st.anchor:
+                # the GPU's first token sits at a near-tie of the oracle's logits
+                assert spec.top2_margin(st.first_logits[None])[0] < BF16_MARGIN
+                continue
+            block = np.concatenate([[st.anchor], proposal[s]])
+            x = _final_residual(m, p, block)
+            lg = m.logits(x, "final_norm")
+            assert _rel_l2(hid[s], x) <= BF16_HIDDEN_REL
+            assert np.abs(vlog[s] - lg).max() <= BF16_LOGIT_TOL
+            checked += 1
+        assert checked >= 1
+    finally:
+        sess.close()
+
+
+def _final_residual(m, prompt, block):
+    """Oracle residual after the last target layer for `block` appended to `prompt`."""
+    c = m.cfg
+    cache = m.new_target_cache()
+    m.target_forward(prompt, cache)
+    tokens = np.asarray(block, dtype=np.int64)
+    n0, n = cache.length, len(tokens)
+    pos = np.arange(n0, n0 + n)
+    x = m.w("embed")[tokens].copy()
+    for l in range(c.target_layers):
+        p = f"t{l}"
+        q, k, v = m._qkv(p, x, pos, c.target_qk_norm)
+        cache.append(l, k, v)
+        visible = np.arange(n0 + n)[None, :] <= pos[:, None]
+        x = m._attn_out_mlp(p, x, om.attention(q, cache.k[l], cache.v[l], visible))
+    return x
+
+
+# ------------------------------------------------------------------ errors
+def test_state_and_capacity_errors():
+    import block_diffusion_speculative_ctx_gb300 as dfl
+    w = configs.get("tiny_f32")
+    sess = _session(w, max_seq_len=48)
+    try:
+        with pytest.raises(dfl.DFlashError) as e:
+            sess.batch = 1
+            sess.draft_block()
+        assert e.value.status == dfl.DFLASH_E_STATE
+        p = synth.prompts(w)[0]
+        sess.prefill([p])
+        with pytest.raises(dfl.DFlashError) as e:
+            sess.verify(np.zeros((1, 3), np.int32))
+        assert e.value.status == dfl.DFLASH_E_STATE
+        sess.draft_block()
+        with pytest.raises(dfl.DFlashError) as e:
+            sess.verify(np.full((1, 3), w.vocab, np.int32))
+        assert e.value.status == dfl.DFLASH_E_INVAL
+        # after the rejected call the drafted state is intact
+        sess.verify(np.zeros((1, 3), np.int32))
+        # fill to capacity: 32 + rounds * (a+1) <= 48 - B
+        with pytest.raises(dfl.DFlashError) as e:
+            for _ in range(20):
+                sess.draft_block()
+                sess.verify(np.zeros((1, 3), np.int32))
+        assert e.value.status == dfl.DFLASH_E_CAPACITY
+    finally:
+        sess.close()
+
+
+def test_device_token_check_reports_without_faulting():
+    import torch
+    import block_diffusion_speculative_ctx_gb300 as dfl
+    w = configs.get("tiny_f32")
+    sess = _session(w)
+    try:
+        sess.prefill([synth.prompts(w)[0]])
+        sess.draft_block()
+        bad = torch.full((1, 3), w.vocab + 5, dtype=torch.int32, device="cuda")
+        with pytest.raises(dfl.DFlashError) as e:
+            sess.verify(bad, np.zeros(1, np.int32), np.zeros(1, np.int32))
+        assert e.value.status == dfl.DFLASH_E_DEVICE_CHECK
+        # the context is still usable
+        sess.draft_block()
+        sess.verify(np.zeros((1, 3), np.int32))
+    finally:
+        sess.close()
