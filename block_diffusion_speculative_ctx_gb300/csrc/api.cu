@@ -21,6 +21,12 @@
 
 using namespace dfl;
 
+static thread_local std::string g_init_error;
+
+namespace dfl {
+void set_global_error(const char* msg) { g_init_error = msg; }
+}  // namespace dfl
+
 namespace {
 
 constexpr int PAGE_TOKENS = 64;
@@ -29,8 +35,6 @@ constexpr int PREFILL_CHUNK = 2048;
 constexpr size_t ATTN_WS_BYTES = 64ull << 20;
 
 enum State { ST_EMPTY = 0, ST_READY = 1, ST_DRAFTED = 2 };
-
-thread_local std::string g_init_error;
 
 struct LayerW {
     void* wqkv = nullptr;   // [(H + 2 Hkv) hd, d]: rows wq, wk, wv

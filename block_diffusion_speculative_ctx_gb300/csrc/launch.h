@@ -104,6 +104,9 @@ void block_rows(const Launch& L, int batch, int B, const int* n, const int* anch
 void accept(const Launch& L, int batch, int B, const int* proposal, const int* posterior, int* n, int* anchor,
             int* accepted, int* bonus, int* ctx_row_seq, int* ctx_row_pos);
 
+// Text returned by dflash_last_error(NULL) (calls that have no session).
+__attribute__((visibility("hidden"))) void set_global_error(const char* msg);
+
 // Gather int32 from a device array by index (used to read the last prompt row's argmax).
 void fill_prefill_rows(const Launch& L, int seq, int start_pos, int rows, int* row_seq, int* row_pos);
 

@@ -255,6 +255,46 @@ dflash_status dflash_inspect(dflash_ctx* ctx, int32_t what, int32_t seq, int32_t
  * headline timings are taken with it off.  Errors: E_INVAL (ctx NULL), E_CUDA. */
 dflash_status dflash_set_profiling(dflash_ctx* ctx, int32_t on);
 
+/* Maximum scratch, in bytes, of dflash_head_argmax_noalloc. */
+enum { DFLASH_NOALLOC_SCRATCH_BYTES = 16 << 20 };
+
+/* Shared-head argmax for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this call; it exists for deployment.  Some
+ * callers cannot call cudaMalloc or any allocator: code running inside
+ * another framework's fixed memory pool, an embedded runtime whose allocator
+ * is locked, or a process whose device memory budget is settled before this
+ * library is loaded.  Such a caller cannot create a session (dflash_init
+ * allocates), but can still pick tokens from final hidden states with this
+ * call: out[r] = argmax_v ( RMSNorm(x[r]) * norm_w ) . head[v], ties to the
+ * lowest id - the same kernels dflash_verify uses for its posterior.
+ *
+ * Arguments (all device pointers except cuda_stream):
+ *   dtype   DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16: element type of head
+ *   x       fp32 [rows, d_model] hidden states (not modified)
+ *   norm_w  fp32 [d_model] RMSNorm scale;  eps: RMSNorm epsilon (> 0)
+ *   head    [vocab, d_model] LM head
+ *   out     int32 [rows] token ids (written)
+ *   cuda_stream  cudaStream_t the kernels are queued on (NULL = legacy default)
+ * The call queues its kernels and returns without synchronising.
+ *
+ * Memory: it allocates nothing.  Its intermediates (the normalised rows and
+ * the fp32 logits, rows * (d_model * elem + vocab * 4) bytes plus alignment)
+ * live in one fixed array of DFLASH_NOALLOC_SCRATCH_BYTES (16 MiB) that every
+ * GPU which loads this library holds until the process exits.  Larger
+ * requests are rejected with DFLASH_E_INVAL before anything is queued (for
+ * example at vocab 151936 and d_model 4096 in bf16, up to 27 rows fit).
+ * The first call on each device looks up that array's device address with
+ * the device current; make that first call before any CUDA stream capture.
+ * All calls share the array and it keeps the last call's contents; no part of
+ * it needs to start at zero.  Calls that overlap on the GPU (on different
+ * streams, or from different threads) race on the array: order them.
+ * Errors: E_INVAL (NULL pointer, bad sizes, request above the maximum),
+ * E_CUDA; the text is available from dflash_last_error(NULL). */
+dflash_status dflash_head_argmax_noalloc(int32_t dtype, const float* x, const float* norm_w, float eps,
+                                         const void* head, int32_t rows, int32_t d_model, int32_t vocab,
+                                         int32_t* out, void* cuda_stream);
+
 /* Release every library-owned buffer.  NULL is a no-op. */
 void dflash_destroy(dflash_ctx* ctx);
 
