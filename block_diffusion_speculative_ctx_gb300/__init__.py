@@ -33,6 +33,7 @@ STATUS_NAMES = {0: "OK", 1: "E_INVAL", 2: "E_NOMEM", 3: "E_CUDA", 4: "E_STATE", 
 DFLASH_DTYPE_F32, DFLASH_DTYPE_BF16 = 0, 1
 DFLASH_FLAG_KEEP_LOGITS = 1
 DFLASH_FLAG_PROFILE = 2
+DFLASH_FLAG_NO_GRAPHS = 4
 KERNEL_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "gemm_fc", "gemm_ctx_kv",
                   "attention", "norm", "rope_store", "swiglu", "argmax", "other")
 DFLASH_MAX_CTX_LAYERS = 16

@@ -33,6 +33,8 @@ constexpr int PAGE_TOKENS = 64;
 constexpr int PAGE_SHIFT = 6;
 constexpr int PREFILL_CHUNK = 2048;
 constexpr size_t ATTN_WS_BYTES = 64ull << 20;
+constexpr size_t GEMM_WS_BYTES = 64ull << 20;
+constexpr int GEMM_COUNTERS = 1 << 16;
 
 enum State { ST_EMPTY = 0, ST_READY = 1, ST_DRAFTED = 2 };
 
@@ -101,6 +103,9 @@ struct dflash_ctx {
     int* drafts = nullptr;
     uint32_t* errw = nullptr;
     float* attn_ws = nullptr;
+    float* gemm_ws = nullptr;
+    int* gemm_counters = nullptr;
+    bool launch_failed = false;
     float* keep_prefill = nullptr;
     float* keep_draft = nullptr;
     float* keep_verify = nullptr;
@@ -122,12 +127,34 @@ struct dflash_ctx {
         double bytes, flops;
     };
     bool profiling = false;
+
+    // CUDA graphs of the draft pass (without / with the context append) and the
+    // verify pass, captured on `cap_stream` and replayed on `stream`
+    struct GraphSlot {
+        cudaGraphExec_t exec = nullptr;
+        int batch = -1;
+        long long kernels = 0;
+        int eager_runs = 0;
+    };
+    GraphSlot g_draft[2], g_verify;
+    cudaStream_t cap_stream = nullptr;
+    bool graphs = true;
     std::vector<cudaEvent_t> prof_ev;
     int prof_next = 0;
     std::vector<ProfRec> prof_pending;
     dflash_profile_entry prof_acc[DFLASH_K_COUNT];
 
-    Launch L() { return Launch{stream, &launches}; }
+    Launch L() {
+        Launch l{stream, &launches};
+        l.ws = gemm_ws;
+        l.ws_bytes = GEMM_WS_BYTES;
+        l.counters = gemm_counters;
+        l.n_counters = GEMM_COUNTERS;
+        l.err = errw;
+        l.failed = &launch_failed;
+        l.pdl = true;
+        return l;
+    }
 
     dflash_status fail(dflash_status s, const char* fmt, ...) {
         char buf[512];
@@ -264,6 +291,7 @@ dflash_status check_device(dflash_ctx* c) {
     CUDA_TRY(c, cudaStreamSynchronize(c->stream));
     if (e) {
         CUDA_TRY(c, cudaMemsetAsync(c->errw, 0, 4, c->stream));
+        if (e & ERR_TIMEOUT) return c->fail(DFLASH_E_TIMEOUT, "a bounded device-side wait ran out (code %u)", e);
         return c->fail(DFLASH_E_DEVICE_CHECK, "device-side check failed (code %u%s%s)", e,
                        (e & ERR_TOKEN_RANGE) ? ": token id outside [0, vocab)" : "",
                        (e & ERR_POSITION_RANGE) ? ": position beyond max_seq_len" : "");
@@ -316,6 +344,8 @@ int attn_group_rows(int rows_per_seq, int g) {
         if (rows_per_seq % r == 0 && r * g <= 64) best = r;
     return best;
 }
+
+dflash_status launch_check(dflash_ctx* c);
 
 // ------------------------------------------------------------ model passes
 template <typename T>
@@ -486,6 +516,8 @@ struct Pass {
             }
             off += P;
         }
+        dflash_status ls = launch_check(c);
+        if (ls != DFLASH_OK) return ls;
         std::vector<int> nh(lens, lens + batch);
         CUDA_TRY(c, cudaMemcpyAsync(c->n, nh.data(), (size_t)batch * 4, cudaMemcpyHostToDevice, c->stream));
         CUDA_TRY(c, cudaMemcpyAsync(first, c->anchor, (size_t)batch * 4, cudaMemcpyDeviceToHost, c->stream));
@@ -505,13 +537,11 @@ struct Pass {
                        c->row_pos, c->errw);
             embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, b * B, c->x, c->errw);
         });
-        int maxk = 0;
+        // attention grid sized from the session capacity, not the current length, so
+        // that the pass is the same launch sequence every round (graph replay)
         double keys = 0;
-        for (int s = 0; s < b; ++s) {
-            maxk = std::max(maxk, c->n_upper[s] + B);
-            keys += c->n_upper[s] + B;
-        }
-        layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), maxk, false, keys);
+        for (int s = 0; s < b; ++s) keys += c->n_upper[s] + B;
+        layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, false, keys);
         head(0, b * B, c->draft_norm, c->argbuf, c->keep_draft);
         // drafts[s][j] = argmax of row s*B + 1 + j
         cudaMemcpy2DAsync(c->drafts, (size_t)(B - 1) * 4, c->argbuf + 1, (size_t)B * 4, (size_t)(B - 1) * 4, b,
@@ -526,13 +556,9 @@ struct Pass {
                        c->row_seq, c->row_pos, c->errw);
             embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, b * B, c->x, c->errw);
         });
-        int maxk = 0;
         double keys = 0;
-        for (int s = 0; s < b; ++s) {
-            maxk = std::max(maxk, c->n_upper[s] + B);
-            keys += c->n_upper[s] + B;
-        }
-        layers(true, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), maxk, true, keys);
+        for (int s = 0; s < b; ++s) keys += c->n_upper[s] + B;
+        layers(true, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, true, keys);
         if (c->keep_hidden)
             cudaMemcpyAsync(c->keep_hidden, c->x, (size_t)b * B * c->d * 4, cudaMemcpyDeviceToDevice, c->stream);
         head(0, b * B, c->final_norm, c->posterior, c->keep_verify);
@@ -560,18 +586,91 @@ dflash_status capacity_check(dflash_ctx* c) {
     return DFLASH_OK;
 }
 
-dflash_status do_draft(dflash_ctx* c) {
-    if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.draft();
-    else Pass<float>{c}.draft();
+dflash_status launch_check(dflash_ctx* c) {
+    if (c->launch_failed) {
+        c->launch_failed = false;
+        return c->fail(DFLASH_E_CUDA, "a tensor-core GEMM could not be prepared (TMA descriptor encode failed)");
+    }
     CUDA_TRY(c, cudaGetLastError());
     return DFLASH_OK;
 }
 
+void reset_graph(dflash_ctx::GraphSlot& g) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    g = dflash_ctx::GraphSlot();
+}
+
+// Run one pass: eagerly the first time (and whenever profiling), then as a
+// captured CUDA graph.  Every launch of a pass reads the round's variable state
+// (lengths, anchors, proposals) from device memory and uses grids fixed by the
+// session's capacity, so a captured pass replays the same work as an eager one.
+template <class F>
+dflash_status run_pass(dflash_ctx* c, dflash_ctx::GraphSlot& g, F&& pass) {
+    if (!c->graphs || c->profiling) {
+        pass();
+        return launch_check(c);
+    }
+    if (g.exec && g.batch == c->batch) {
+        CUDA_TRY(c, cudaGraphLaunch(g.exec, c->stream));
+        c->launches += g.kernels;
+        // host-side effects of the pass
+        return DFLASH_OK;
+    }
+    if (g.batch != c->batch) {
+        reset_graph(g);
+        g.batch = c->batch;
+    }
+    if (g.eager_runs < 1) {
+        ++g.eager_runs;
+        pass();
+        return launch_check(c);
+    }
+    // capture on the library's own stream, ordered after the caller's stream
+    cudaStream_t user = c->stream;
+    CUDA_TRY(c, cudaEventRecord(c->ev[3], user));
+    CUDA_TRY(c, cudaStreamWaitEvent(c->cap_stream, c->ev[3], 0));
+    CUDA_TRY(c, cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+    c->stream = c->cap_stream;
+    const long long l0 = c->launches;
+    pass();
+    c->stream = user;
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(c->cap_stream, &graph);
+    if (e != cudaSuccess || !graph) return c->fail(DFLASH_E_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+    dflash_status ls = launch_check(c);
+    if (ls != DFLASH_OK) {
+        cudaGraphDestroy(graph);
+        return ls;
+    }
+    e = cudaGraphInstantiate(&g.exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+        g.exec = nullptr;
+        return c->fail(DFLASH_E_CUDA, "graph instantiation failed: %s", cudaGetErrorString(e));
+    }
+    g.kernels = c->launches - l0;
+    CUDA_TRY(c, cudaGraphLaunch(g.exec, c->stream));
+    return DFLASH_OK;
+}
+
+dflash_status do_draft(dflash_ctx* c) {
+    const int with_append = c->pending_append ? 1 : 0;
+    dflash_status s = run_pass(c, c->g_draft[with_append], [&] {
+        if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.draft();
+        else Pass<float>{c}.draft();
+    });
+    c->pending_append = false;
+    return s;
+}
+
 dflash_status do_verify(dflash_ctx* c) {
-    if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.verify();
-    else Pass<float>{c}.verify();
-    CUDA_TRY(c, cudaGetLastError());
-    for (int s = 0; s < c->batch; ++s) c->n_upper[s] += c->B;
+    dflash_status s = run_pass(c, c->g_verify, [&] {
+        if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.verify();
+        else Pass<float>{c}.verify();
+    });
+    if (s != DFLASH_OK) return s;
+    c->pending_append = true;
+    for (int i = 0; i < c->batch; ++i) c->n_upper[i] += c->B;
     return DFLASH_OK;
 }
 
@@ -744,6 +843,8 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     ALLOC(c->drafts, (size_t)cfg->max_batch * c->B * 4);
     ALLOC(c->errw, 16);
     ALLOC(c->attn_ws, ATTN_WS_BYTES);
+    ALLOC(c->gemm_ws, GEMM_WS_BYTES);
+    ALLOC(c->gemm_counters, (size_t)GEMM_COUNTERS * 4);
     if (cfg->flags & DFLASH_FLAG_KEEP_LOGITS) {
         ALLOC(c->keep_prefill, (size_t)cfg->max_batch * V * 4);
         ALLOC(c->keep_draft, (size_t)rb * V * 4);
@@ -751,6 +852,7 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
         ALLOC(c->keep_hidden, (size_t)rb * d * 4);
     }
     if (cudaMemsetAsync(c->errw, 0, 16, c->stream) != cudaSuccess ||
+        cudaMemsetAsync(c->gemm_counters, 0, (size_t)GEMM_COUNTERS * 4, c->stream) != cudaSuccess ||
         cudaMemsetAsync(c->n, 0, (size_t)cfg->max_batch * 4, c->stream) != cudaSuccess) {
         c->fail(DFLASH_E_CUDA, "memset failed");
         return bail(DFLASH_E_CUDA);
@@ -761,6 +863,11 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
             return bail(DFLASH_E_CUDA);
         }
     c->events = true;
+    if (cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        c->fail(DFLASH_E_CUDA, "stream creation failed");
+        return bail(DFLASH_E_CUDA);
+    }
+    c->graphs = (cfg->flags & DFLASH_FLAG_NO_GRAPHS) == 0;
     memset(c->prof_acc, 0, sizeof c->prof_acc);
     if ((cfg->flags & DFLASH_FLAG_PROFILE) && dflash_set_profiling(c, 1) != DFLASH_OK) return bail(DFLASH_E_CUDA);
     if (cudaStreamSynchronize(c->stream) != cudaSuccess) {
@@ -1001,6 +1108,10 @@ void dflash_destroy(dflash_ctx* c) {
     if (c->events)
         for (int i = 0; i < 4; ++i) cudaEventDestroy(c->ev[i]);
     for (auto& e : c->prof_ev) cudaEventDestroy(e);
+    reset_graph(c->g_draft[0]);
+    reset_graph(c->g_draft[1]);
+    reset_graph(c->g_verify);
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
     delete c;
 }
 

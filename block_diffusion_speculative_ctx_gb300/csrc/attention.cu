@@ -32,6 +32,8 @@ struct AttnArgs {
 
 template <typename T, int HD>
 __global__ void __launch_bounds__(NT) attn_kernel(AttnArgs a) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ float sm[];
     constexpr int QLD = HD + 1, SLD = KT + 1;   // padded rows: no shared-memory bank conflicts
     float* Qs = sm;                       // [QV][QLD]
@@ -208,6 +210,8 @@ __global__ void __launch_bounds__(NT) attn_kernel(AttnArgs a) {
 
 template <typename T, int HD>
 __global__ void attn_combine_kernel(AttnArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const AttnParams& p = a.p;
     const int r = blockIdx.x, h = blockIdx.y;
     if (p.row_seq[r] < 0) return;
@@ -259,12 +263,8 @@ void run(const Launch& L, const AttnParams& p) {
         attr_set = true;
     }
     dim3 grid(a.n_groups, p.Hkv, splits);
-    attn_kernel<T, HD><<<grid, NT, smem, L.stream>>>(a);
-    L.bump();
-    if (splits > 1) {
-        attn_combine_kernel<T, HD><<<dim3(p.rows, p.H), HD, 0, L.stream>>>(a);
-        L.bump();
-    }
+    launch_k(L, attn_kernel<T, HD>, grid, dim3(NT), smem, 1, a);
+    if (splits > 1) launch_k(L, attn_combine_kernel<T, HD>, dim3(p.rows, p.H), dim3(HD), 0, 1, a);
 }
 
 }  // namespace

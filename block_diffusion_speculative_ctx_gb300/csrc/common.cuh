@@ -60,6 +60,15 @@ enum : uint32_t {
     ERR_TIMEOUT = 4u
 };
 
+// ---- programmatic dependent launch -------------------------------------------
+// Every kernel of the round may be launched so that it starts while the kernel
+// before it is still running.  pdl_wait() blocks until that kernel has finished
+// and its writes are visible; each kernel calls it in every thread before it
+// reads anything an earlier kernel wrote (and before it can exit), so kernel
+// completion stays ordered.  pdl_trigger() lets the next kernel start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- paged KV addressing ---------------------------------------------------
 // A cache layer is [num_pages][H_kv][page_tokens][hd]; page_table[seq * pages_per_seq + i]
 // gives the physical page of the seq's i-th block of page_tokens positions.

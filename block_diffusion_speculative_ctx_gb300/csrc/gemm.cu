@@ -1,7 +1,7 @@
 // CUDA-core GEMM C[M, N] (=|+=) A[M, K] . W[N, K]^T with fp32 accumulation.
 //
-// This is the fp32 path (FP32 FMA, no TF32) and the reference-grade fallback
-// shape for bf16 operands.  Each output element is one dot product reduced in
+// This is the fp32 path (FP32 FMA, no TF32); bf16 operands go to the tcgen05
+// kernel in gemm_tc.cu.  Each output element is one dot product reduced in
 // a fixed k order that does not depend on M, so a row's result is the same
 // whether it is computed alone or with other rows.
 #include "launch.h"
@@ -30,6 +30,8 @@ template <typename T, int BM, int BN, int BK, int TM, int TN>
 __global__ void __launch_bounds__((BM / TM) * (BN / TN))
     gemm_cc_kernel(const T* __restrict__ A, int lda, const T* __restrict__ W, float* __restrict__ C, int ldc, int M,
                    int N, int K, int accumulate) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int NTX = BN / TN, NTY = BM / TM, NT = NTX * NTY;
     __shared__ __align__(16) float As[BK][BM + 4];
     __shared__ __align__(16) float Ws[BK][BN + 4];
@@ -96,21 +98,32 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
 }  // namespace
 
 template <typename T>
-void gemm(const Launch& L, const T* A, int lda, const T* W, int M, int N, int K, float* C, int ldc, bool accumulate) {
+void gemm_cc(const Launch& L, const T* A, int lda, const T* W, int M, int N, int K, float* C, int ldc, bool accumulate) {
     if (M <= 0 || N <= 0) return;
     if (M <= 16) {
         constexpr int BM = 16, BN = 128;
         dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
-        gemm_cc_kernel<T, BM, BN, 32, 2, 4><<<grid, 256, 0, L.stream>>>(A, lda, W, C, ldc, M, N, K, accumulate);
+        launch_k(L, gemm_cc_kernel<T, BM, BN, 32, 2, 4>, grid, dim3(256), 0, 1, A, lda, W, C, ldc, M, N, K,
+                 (int)accumulate);
     } else {
         constexpr int BM = 64, BN = 64;
         dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
-        gemm_cc_kernel<T, BM, BN, 32, 4, 4><<<grid, 256, 0, L.stream>>>(A, lda, W, C, ldc, M, N, K, accumulate);
+        launch_k(L, gemm_cc_kernel<T, BM, BN, 32, 4, 4>, grid, dim3(256), 0, 1, A, lda, W, C, ldc, M, N, K,
+                 (int)accumulate);
     }
-    L.bump();
 }
 
-template void gemm<float>(const Launch&, const float*, int, const float*, int, int, int, float*, int, bool);
-template void gemm<bf16>(const Launch&, const bf16*, int, const bf16*, int, int, int, float*, int, bool);
+template <>
+void gemm<float>(const Launch& L, const float* A, int lda, const float* W, int M, int N, int K, float* C, int ldc,
+                 bool accumulate) {
+    gemm_cc<float>(L, A, lda, W, M, N, K, C, ldc, accumulate);
+}
+
+template <>
+void gemm<bf16>(const Launch& L, const bf16* A, int lda, const bf16* W, int M, int N, int K, float* C, int ldc,
+                bool accumulate) {
+    if (M <= 0 || N <= 0) return;
+    if (!gemm_tc(L, A, lda, M, W, M, N, K, C, ldc, accumulate)) L.fail();
+}
 
 }  // namespace dfl

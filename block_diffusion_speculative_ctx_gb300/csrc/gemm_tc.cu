@@ -1,0 +1,515 @@
+// Tensor-core GEMM for bf16 operands on sm_103a (tcgen05 + TMA + TMEM):
+//
+//     C[M, N] (fp32, row stride ldc)  =|+=  A[M, K] (bf16) . W[N, K]^T (bf16)
+//
+// The weight matrix is the MMA's A operand: each CTA owns a 128-row slab of W
+// (128 output features) and one range of K; the activations (the M token rows,
+// at most 256 per tile) are the B operand, so the accumulator D[128, M_tile]
+// lives in TMEM with one output feature per lane.  This "swap" keeps the
+// tensor cores usable when M is only a block of 16 tokens: the work is the
+// weight stream, and every weight byte is read from HBM once.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads (one elected lane), warp 1
+// allocates TMEM and issues tcgen05.mma (one elected lane), warps 2-5 drain the
+// accumulator (tcgen05.ld; warp w reads TMEM lanes 32*(w%4) .. +31).  A ring of
+// STAGES shared-memory stages (128-byte swizzled, as TMA writes them and as
+// the UMMA descriptors read them) is guarded by full/empty mbarriers.
+//
+// Split-K: when the N tiles alone cannot fill the GPU, K is cut into `splits`
+// (<= 8) contiguous ranges whose CTAs form one thread-block cluster.  Each CTA
+// parks its fp32 partial tile in its own shared memory; after a cluster
+// barrier, CTA r sums columns [r*MT/S, (r+1)*MT/S) of the tile over the peers'
+// shared memory (distributed shared memory), always in rank order, so the
+// result does not depend on scheduling, and applies the epilogue.
+//
+// Programmatic dependent launch: the producer fills the first STAGES weight
+// tiles before waiting for the previous kernel (weights never depend on it),
+// so the weight stream of this GEMM overlaps the tail of the kernel before.
+//
+// Every wait on an mbarrier is bounded; a wait that runs out sets ERR_TIMEOUT
+// in the error word, and the CTA still reaches its cluster barriers, releases
+// its TMEM and returns.
+#include <cuda.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "launch.h"
+
+namespace dfl {
+
+namespace {
+
+constexpr int BN = 128;          // weight rows per tile = UMMA M
+constexpr int BK = 64;           // K per stage: one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;
+constexpr int THREADS = 192;
+constexpr uint32_t WAIT_LIMIT = 1u << 26;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i >= 1024) __nanosleep(128);
+    }
+    if (err) atomicOr(err, ERR_TIMEOUT);
+    return false;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 2-D tiled TMA load: coordinates {c0 = element along the contiguous dim, c1 = row}.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// UMMA shared-memory descriptor: K-major operand in the 128-byte swizzle
+// layout TMA produces (rows of 128 B, 8-row atoms 1024 B apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address, 16-byte units
+    d |= (uint64_t)1 << 16;                     // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: next 8-row atom
+    d |= (uint64_t)1 << 46;                     // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                     // swizzle mode: 128 B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+    return (1u << 4)                      // D format fp32
+           | (1u << 7)                    // A format bf16
+           | (1u << 10)                   // B format bf16
+           | ((uint32_t)(n >> 3) << 17)   // N / 8
+           | ((uint32_t)(BN >> 4) << 24); // M / 16
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 16 consecutive fp32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// fp32 load from the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+struct TcArgs {
+    float* C;
+    int ldc, M, N, K;
+    int accumulate;
+    int splits;
+    int kb_per_split;
+    int n_tiles;
+    uint32_t* err;
+};
+
+template <int MT, int STAGES>
+struct Smem {
+    static constexpr int W_BYTES = BN * BK * 2;   // 16 KB
+    static constexpr int X_BYTES = MT * BK * 2;
+    static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr int TOTAL = BAR_OFF + (2 * STAGES + 1) * 8 + 16 + 1024;  // + alignment slack
+};
+
+template <int MT, int STAGES>
+__global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                          const __grid_constant__ CUtensorMap tmX, TcArgs a) {
+    using S = Smem<MT, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled tiles
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+    uint64_t* empty = full + STAGES;
+    uint64_t* accf = empty + STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nt = blockIdx.x, mt = blockIdx.y, split = blockIdx.z;
+    const int n0 = nt * BN, m0 = mt * MT;
+    const int KB = (a.K + BK - 1) / BK;
+    const int kb0 = split * a.kb_per_split;
+    const int kb1 = min(KB, kb0 + a.kb_per_split);
+    const int nkb = kb1 - kb0;
+    constexpr uint32_t TMEM_COLS = MT < 32 ? 32 : MT;
+
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accf, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    pdl_trigger();  // the next kernel may start its own prologue now
+
+    bool ok = true;
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+            // weights of the first stages do not depend on the previous kernel
+            const int pre = nkb < STAGES ? nkb : STAGES;
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], S::STAGE_BYTES);
+                tma_load_2d(smem + i * S::STAGE_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0, pw);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(smem + i * S::STAGE_BYTES + S::W_BYTES, &tmX, &full[i], (kb0 + i) * BK, m0, px);
+            for (int i = pre; i < nkb; ++i) {
+                const int s = i % STAGES;
+                if (!mbar_wait(&empty[s], ((i / STAGES) + 1) & 1, a.err)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = smem + s * S::STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
+                const int kc = (kb0 + i) * BK;
+                tma_load_2d(st, &tmW, &full[s], kc, n0, pw);
+                tma_load_2d(st + S::W_BYTES, &tmX, &full[s], kc, m0, px);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(MT);
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % STAGES;
+                if (!mbar_wait(&full[s], (i / STAGES) & 1, a.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sw = smem_u32(smem + s * S::STAGE_BYTES);
+                const uint32_t sx = sw + S::W_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                    umma_bf16(tmem, sw128_desc(sw + kk * UMMA_K * 2), sw128_desc(sx + kk * UMMA_K * 2), idesc,
+                              (i > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&empty[s]);
+            }
+            umma_commit(accf);  // fires once every MMA issued above has completed
+        }
+    }
+    __syncwarp();
+    pdl_wait();  // every thread: the previous kernel's outputs (C when accumulating) are visible
+
+    const int q = warp & 3;
+    const int row = 32 * q + lane;  // feature within the tile
+    const int n = n0 + row;
+    float* part = reinterpret_cast<float*>(smem);  // [MT][BN] partial tile (stage memory is free by then)
+    if (warp >= 2) {
+        // one lane waits; the warp then runs the .sync.aligned TMEM loads together
+        uint32_t okw = 0;
+        if (lane == 0) okw = mbar_wait(accf, 0, a.err) ? 1u : 0u;
+        ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
+        tc_fence_after();
+        const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
+        float v[16];
+#pragma unroll
+        for (int c = 0; c < MT; c += 16) {
+            if (ok) tmem_ld16(tbase + c, v);
+            else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            }
+            if (a.splits == 1) {
+                if (n < a.N) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = m0 + c + j;
+                        if (m < a.M) {
+                            float* dst = a.C + (size_t)m * a.ldc + n;
+                            *dst = a.accumulate ? (*dst + v[j]) : v[j];
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) part[(c + j) * BN + row] = v[j];
+            }
+        }
+    }
+
+    if (a.splits > 1) {
+        // ---- cluster split-K: rank r reduces its slice of columns over all ranks, in rank order
+        cluster_sync();
+        const uint32_t rank = cluster_rank();
+        const int per = (MT + a.splits - 1) / a.splits;
+        const int j0 = (int)rank * per;
+        const int j1 = min(MT, j0 + per);
+        if (warp >= 2 && n < a.N) {
+            for (int j = j0; j < j1; ++j) {
+                const int m = m0 + j;
+                if (m >= a.M) break;
+                float vals[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) vals[r] = (r < a.splits) ? ld_peer(part + j * BN + row, (uint32_t)r) : 0.f;
+                float acc = 0.f;
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (r < a.splits) acc += vals[r];
+                float* dst = a.C + (size_t)m * a.ldc + n;
+                *dst = a.accumulate ? (*dst + acc) : acc;
+            }
+        }
+        cluster_sync();  // peers keep their shared memory until every slice is read
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void* ptr;
+    long long rows, cols, ld;
+    int box_rows;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && box_rows == o.box_rows;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        size_t h = std::hash<const void*>()(k.ptr);
+        h ^= std::hash<long long>()(k.rows * 1000003LL + k.cols) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+        h ^= std::hash<long long>()(k.ld * 131 + k.box_rows) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+        return h;
+    }
+};
+
+// Tensor map of a row-major bf16 matrix [rows, cols] (row stride ld elements),
+// box [box_rows, 64], 128-byte swizzle; out-of-range elements read as zero.
+bool make_map(CUtensorMap* out, const void* ptr, long long rows, long long cols, long long ld, int box_rows) {
+    static std::mutex mu;
+    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+    const MapKey key{ptr, rows, cols, ld, box_rows};
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+        *out = it->second;
+        return true;
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUtensorMap m;
+    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    if (cache.size() > 65536) cache.clear();
+    cache.emplace(key, m);
+    *out = m;
+    return true;
+}
+
+int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+// Split count (cluster size, <= 8) that best fills `slots` concurrent CTAs
+// while keeping at least four K blocks per split.
+int choose_splits(int tiles, int kb, int slots) {
+    int best = 1;
+    double best_eff = 0.0;
+    for (int s = 1; s <= 8; ++s) {
+        if (s > 1 && kb / s < 4) break;
+        const int kbps = (kb + s - 1) / s;
+        const int real = (kb + kbps - 1) / kbps;
+        const long long ctas = (long long)tiles * real;
+        const long long waves = (ctas + slots - 1) / slots;
+        const double eff = (double)ctas / (double)(waves * slots);
+        if (eff > best_eff + 0.03) {
+            best_eff = eff;
+            best = s;
+        }
+    }
+    return best;
+}
+
+template <int MT, int STAGES>
+bool launch_tc(const Launch& L, const CUtensorMap& mw, const CUtensorMap& mx, TcArgs a, int m_tiles) {
+    using S = Smem<MT, STAGES>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(tc_gemm_kernel<MT, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL) !=
+            cudaSuccess)
+            return false;
+        cudaFuncSetAttribute(tc_gemm_kernel<MT, STAGES>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+        attr = true;
+    }
+    const int KB = (a.K + BK - 1) / BK;
+    const int cta_per_sm = S::TOTAL <= 110 * 1024 ? 2 : 1;
+    const int splits = choose_splits(a.n_tiles * m_tiles, KB, sm_count() * cta_per_sm);
+    a.kb_per_split = (KB + splits - 1) / splits;
+    a.splits = (KB + a.kb_per_split - 1) / a.kb_per_split;
+    dim3 grid(a.n_tiles, m_tiles, a.splits);
+    launch_k(L, tc_gemm_kernel<MT, STAGES>, grid, dim3(THREADS), (size_t)S::TOTAL, a.splits, mw, mx, a);
+    return true;
+}
+
+}  // namespace
+
+// bf16 GEMM on the tensor cores.  Returns false when a tensor map cannot be
+// built (the caller reports the error); nothing is launched in that case.
+bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W, int M, int N, int K, float* C,
+             int ldc, bool accumulate) {
+    int MT;
+    if (M <= 16) MT = 16;
+    else if (M <= 32) MT = 32;
+    else if (M <= 64) MT = 64;
+    else if (M <= 128) MT = 128;
+    else MT = 256;
+    CUtensorMap mw, mx;
+    if (!make_map(&mw, W, N, K, K, BN)) return false;
+    if (!make_map(&mx, A, a_rows, K, lda, MT)) return false;
+    TcArgs a;
+    a.C = C;
+    a.ldc = ldc;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.accumulate = accumulate ? 1 : 0;
+    a.n_tiles = (N + BN - 1) / BN;
+    a.err = L.err;
+    a.splits = 1;
+    a.kb_per_split = 0;
+    const int m_tiles = (M + MT - 1) / MT;
+    switch (MT) {
+        case 16: return launch_tc<16, 6>(L, mw, mx, a, m_tiles);
+        case 32: return launch_tc<32, 5>(L, mw, mx, a, m_tiles);
+        case 64: return launch_tc<64, 4>(L, mw, mx, a, m_tiles);
+        case 128: return launch_tc<128, 4>(L, mw, mx, a, m_tiles);
+        default: return launch_tc<256, 4>(L, mw, mx, a, m_tiles);
+    }
+}
+
+}  // namespace dfl

@@ -9,6 +9,8 @@ namespace dfl {
 template <typename T>
 __global__ void embed_kernel(const int* __restrict__ tokens, const T* __restrict__ embed, int vocab, int d,
                              float* __restrict__ x, uint32_t* err) {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x;
     int t = tokens[r];
     if (t < 0 || t >= vocab) {
@@ -24,8 +26,7 @@ template <typename T>
 void embed_rows(const Launch& L, const int* tokens, const T* embed, int vocab, int d, int rows, float* x,
                 uint32_t* err) {
     if (rows <= 0) return;
-    embed_kernel<T><<<rows, 256, 0, L.stream>>>(tokens, embed, vocab, d, x, err);
-    L.bump();
+    launch_k(L, embed_kernel<T>, dim3(rows), dim3(256), 0, 1, tokens, embed, vocab, d, x, err);
 }
 
 // ------------------------------------------------------------------ RMSNorm
@@ -33,6 +34,8 @@ void embed_rows(const Launch& L, const int* tokens, const T* embed, int vocab, i
 template <typename T>
 __global__ void rmsnorm_kernel(const float* __restrict__ x, int ldx, const int* __restrict__ row_idx,
                                const float* __restrict__ w, int d, float eps, T* __restrict__ out, int ldo) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[32];
     const int r = blockIdx.x;
     const int src_row = row_idx ? row_idx[r] : r;
@@ -52,16 +55,14 @@ template <typename T>
 void rmsnorm_rows(const Launch& L, const float* x, int ldx, const float* w, int rows, int d, float eps, T* out,
                   int ldo) {
     if (rows <= 0) return;
-    rmsnorm_kernel<T><<<rows, 256, 0, L.stream>>>(x, ldx, nullptr, w, d, eps, out, ldo);
-    L.bump();
+    launch_k(L, rmsnorm_kernel<T>, dim3(rows), dim3(256), 0, 1, x, ldx, (const int*)nullptr, w, d, eps, out, ldo);
 }
 
 template <typename T>
 void rmsnorm_gather(const Launch& L, const float* x, int ldx, const int* row_idx, const float* w, int rows, int d,
                     float eps, T* out, int ldo) {
     if (rows <= 0) return;
-    rmsnorm_kernel<T><<<rows, 256, 0, L.stream>>>(x, ldx, row_idx, w, d, eps, out, ldo);
-    L.bump();
+    launch_k(L, rmsnorm_kernel<T>, dim3(rows), dim3(256), 0, 1, x, ldx, row_idx, w, d, eps, out, ldo);
 }
 
 // ------------------------------------------------- q/k norm, RoPE, KV store
@@ -70,6 +71,8 @@ void rmsnorm_gather(const Launch& L, const float* x, int ldx, const int* row_idx
 // element j is j + hd/2, i.e. the same lane at i + hd/64.
 template <typename T, int HD>
 __global__ void qkv_store_kernel(QKVStore p) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int PER = HD / 32;    // elements per lane
     constexpr int HALF = PER / 2;   // pair offset in i
     const int r = blockIdx.x;
@@ -132,16 +135,17 @@ void qk_norm_rope_store(const Launch& L, const QKVStore& p) {
     const int nheads = (p.q_off >= 0 ? p.H : 0) + 2 * p.Hkv;
     int warps = nheads < 16 ? nheads : 16;
     if (p.hd == 128)
-        qkv_store_kernel<T, 128><<<p.rows, 32 * warps, 0, L.stream>>>(p);
+        launch_k(L, qkv_store_kernel<T, 128>, dim3(p.rows), dim3(32 * warps), 0, 1, p);
     else
-        qkv_store_kernel<T, 64><<<p.rows, 32 * warps, 0, L.stream>>>(p);
-    L.bump();
+        launch_k(L, qkv_store_kernel<T, 64>, dim3(p.rows), dim3(32 * warps), 0, 1, p);
 }
 
 // -------------------------------------------------------------------- SwiGLU
 // gu = [gate | up] per row (2F fp32); out = silu(gate) * up.
 template <typename T>
 __global__ void silu_mul_kernel(const float* __restrict__ gu, int F, int rows, T* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const size_t n = (size_t)rows * F;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const size_t r = i / F, f = i % F;
@@ -156,13 +160,14 @@ void silu_mul(const Launch& L, const float* gu, int F, int rows, T* out) {
     size_t n = (size_t)rows * F;
     int blocks = (int)((n + 255) / 256);
     if (blocks > 152 * 16) blocks = 152 * 16;
-    silu_mul_kernel<T><<<blocks, 256, 0, L.stream>>>(gu, F, rows, out);
-    L.bump();
+    launch_k(L, silu_mul_kernel<T>, dim3(blocks), dim3(256), 0, 1, gu, F, rows, out);
 }
 
 // ------------------------------------------------------------------ capture
 template <typename T>
 __global__ void capture_kernel(const float* __restrict__ x, int d, T* __restrict__ stage, int ld, int col) {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x;
     for (int c = threadIdx.x; c < d; c += blockDim.x) stage[(size_t)r * ld + col + c] = from_f32<T>(x[(size_t)r * d + c]);
 }
@@ -170,12 +175,13 @@ __global__ void capture_kernel(const float* __restrict__ x, int d, T* __restrict
 template <typename T>
 void capture_rows(const Launch& L, const float* x, int d, int rows, T* stage, int ld_stage, int col) {
     if (rows <= 0) return;
-    capture_kernel<T><<<rows, 256, 0, L.stream>>>(x, d, stage, ld_stage, col);
-    L.bump();
+    launch_k(L, capture_kernel<T>, dim3(rows), dim3(256), 0, 1, x, d, stage, ld_stage, col);
 }
 
 // ------------------------------------------------------------------- argmax
 __global__ void argmax_kernel(const float* __restrict__ logits, long long ld, int V, int* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ unsigned long long red[32];
     const int r = blockIdx.x;
     const float* row = logits + (size_t)r * ld;
@@ -205,8 +211,7 @@ __global__ void argmax_kernel(const float* __restrict__ logits, long long ld, in
 
 void argmax_rows(const Launch& L, const float* logits, long long ld, int rows, int V, int* out) {
     if (rows <= 0) return;
-    argmax_kernel<<<rows, 1024, 0, L.stream>>>(logits, ld, V, out);
-    L.bump();
+    launch_k(L, argmax_kernel, dim3(rows), dim3(1024), 0, 1, logits, ld, V, out);
 }
 
 // --------------------------------------------------------- round bookkeeping
@@ -214,6 +219,8 @@ __global__ void block_rows_kernel(int batch, int B, const int* __restrict__ n, c
                                   const int* __restrict__ proposal, int mask, int vocab, int max_pos,
                                   int* __restrict__ tokens, int* __restrict__ row_seq, int* __restrict__ row_pos,
                                   uint32_t* err) {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= batch * B) return;
     const int s = r / B, j = r % B;
@@ -235,15 +242,16 @@ __global__ void block_rows_kernel(int batch, int B, const int* __restrict__ n, c
 void block_rows(const Launch& L, int batch, int B, const int* n, const int* anchor, const int* proposal, int mask,
                 int vocab, int max_pos, int* tokens, int* row_seq, int* row_pos, uint32_t* err) {
     const int rows = batch * B;
-    block_rows_kernel<<<(rows + 127) / 128, 128, 0, L.stream>>>(batch, B, n, anchor, proposal, mask, vocab,
-                                                                  max_pos, tokens, row_seq, row_pos, err);
-    L.bump();
+    launch_k(L, block_rows_kernel, dim3((rows + 127) / 128), dim3(128), 0, 1, batch, B, n, anchor, proposal, mask,
+             vocab, max_pos, tokens, row_seq, row_pos, err);
 }
 
 // One thread per sequence: the longest prefix with proposal[j] == posterior[j].
 __global__ void accept_kernel(int batch, int B, const int* __restrict__ proposal, const int* __restrict__ posterior,
                               int* __restrict__ n, int* __restrict__ anchor, int* __restrict__ accepted,
                               int* __restrict__ bonus, int* __restrict__ ctx_row_seq, int* __restrict__ ctx_row_pos) {
+    pdl_wait();
+    pdl_trigger();
     const int s = blockIdx.x * blockDim.x + threadIdx.x;
     if (s >= batch) return;
     const int* d = proposal + (size_t)s * (B - 1);
@@ -264,12 +272,13 @@ __global__ void accept_kernel(int batch, int B, const int* __restrict__ proposal
 
 void accept(const Launch& L, int batch, int B, const int* proposal, const int* posterior, int* n, int* anchor,
             int* accepted, int* bonus, int* ctx_row_seq, int* ctx_row_pos) {
-    accept_kernel<<<(batch + 63) / 64, 64, 0, L.stream>>>(batch, B, proposal, posterior, n, anchor, accepted, bonus,
-                                                          ctx_row_seq, ctx_row_pos);
-    L.bump();
+    launch_k(L, accept_kernel, dim3((batch + 63) / 64), dim3(64), 0, 1, batch, B, proposal, posterior, n, anchor,
+             accepted, bonus, ctx_row_seq, ctx_row_pos);
 }
 
 __global__ void prefill_rows_kernel(int seq, int start, int rows, int* row_seq, int* row_pos) {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r < rows) {
         row_seq[r] = seq;
@@ -278,8 +287,7 @@ __global__ void prefill_rows_kernel(int seq, int start, int rows, int* row_seq, 
 }
 
 void fill_prefill_rows(const Launch& L, int seq, int start_pos, int rows, int* row_seq, int* row_pos) {
-    prefill_rows_kernel<<<(rows + 255) / 256, 256, 0, L.stream>>>(seq, start_pos, rows, row_seq, row_pos);
-    L.bump();
+    launch_k(L, prefill_rows_kernel, dim3((rows + 255) / 256), dim3(256), 0, 1, seq, start_pos, rows, row_seq, row_pos);
 }
 
 // ---- explicit instantiations

@@ -12,16 +12,62 @@ namespace dfl {
 
 struct Launch {
     cudaStream_t stream;
-    long long* launches;  // incremented once per kernel launch
+    long long* launches;        // incremented once per kernel launch (may be null)
+    float* ws = nullptr;        // split-K partial tiles (null: no split-K)
+    size_t ws_bytes = 0;
+    int* counters = nullptr;    // split-K tile counters, zero between launches
+    int n_counters = 0;
+    uint32_t* err = nullptr;    // device error word
+    bool* failed = nullptr;     // host flag: a launch could not be prepared
+    bool pdl = false;           // launch with programmatic stream serialization
     void bump(int n = 1) const {
         if (launches) *launches += n;
     }
+    void fail() const {
+        if (failed) *failed = true;
+    }
 };
+
+// Launch `kernel` on L.stream with cudaLaunchKernelEx: programmatic dependent
+// launch when L.pdl is set, and a (1, 1, cluster_z) thread-block cluster when
+// cluster_z > 1.  Counts the launch; a launch error sets the host flag.
+template <typename... KArgs, typename... Args>
+void launch_k(const Launch& L, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, int cluster_z,
+              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (L.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_z > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 1;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = (unsigned)cluster_z;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) L.fail();
+    L.bump();
+}
 
 // ---- GEMM: C[M, N] (fp32, row stride ldc) = or += A[M, K] (T, stride lda) . W[N, K]^T.
 // K, lda and the W row length are multiples of 8; A and W are 16-byte aligned.
+// bf16 runs on the tensor cores (gemm_tc.cu), fp32 on CUDA-core FMA (gemm.cu).
 template <typename T>
 void gemm(const Launch& L, const T* A, int lda, const T* W, int M, int N, int K, float* C, int ldc, bool accumulate);
+
+// tcgen05 GEMM for bf16; false when it could not be launched (tensor map encode failed).
+bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W, int M, int N, int K, float* C,
+             int ldc, bool accumulate);
 
 // ---- row kernels
 template <typename T>

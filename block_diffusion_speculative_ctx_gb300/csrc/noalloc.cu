@@ -54,6 +54,8 @@ template <typename T>
 void run_head(const float* x, const float* norm_w, float eps, const void* head, int rows, int d, int vocab, int* out,
               unsigned char* scratch, cudaStream_t stream) {
     Launch L{stream, nullptr};
+    L.err = reinterpret_cast<uint32_t*>(scratch);  // first 256 bytes: device error word
+    scratch += 256;
     T* xn = reinterpret_cast<T*>(scratch);
     const size_t xn_bytes = ((size_t)rows * d * sizeof(T) + 255) / 256 * 256;
     float* logits = reinterpret_cast<float*>(scratch + xn_bytes);
@@ -72,7 +74,7 @@ extern "C" dflash_status dflash_head_argmax_noalloc(int32_t dtype, const float* 
     if (rows < 1 || d_model < 8 || d_model % 8 || vocab < 1 || !(eps > 0.f))
         return fail(DFLASH_E_INVAL, "rows >= 1, d_model a positive multiple of 8, vocab >= 1 and eps > 0 required");
     const size_t esz = dtype == DFLASH_DTYPE_BF16 ? 2 : 4;
-    const size_t need = ((size_t)rows * d_model * esz + 255) / 256 * 256 + (size_t)rows * vocab * 4;
+    const size_t need = 256 + ((size_t)rows * d_model * esz + 255) / 256 * 256 + (size_t)rows * vocab * 4;
     if (need > NOALLOC_SCRATCH_BYTES) {
         char buf[256];
         snprintf(buf, sizeof buf,

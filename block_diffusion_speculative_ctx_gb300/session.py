@@ -8,7 +8,8 @@ from typing import Optional, Sequence
 
 import numpy as np
 
-from . import (ALLOC_FN, DFLASH_DTYPE_BF16, DFLASH_DTYPE_F32, DFLASH_FLAG_KEEP_LOGITS, DFLASH_OK, FREE_FN,
+from . import (ALLOC_FN, DFLASH_DTYPE_BF16, DFLASH_DTYPE_F32, DFLASH_FLAG_KEEP_LOGITS, DFLASH_FLAG_NO_GRAPHS,
+               DFLASH_OK, FREE_FN,
                INSPECT_ANCHORS, INSPECT_DRAFT_K, INSPECT_DRAFT_V, INSPECT_HIDDEN_VERIFY, INSPECT_LENGTHS,
                INSPECT_LOGITS_DRAFT, INSPECT_LOGITS_PREFILL, INSPECT_LOGITS_VERIFY, INSPECT_POSTERIOR,
                INSPECT_STATS, INSPECT_TARGET_K, INSPECT_TARGET_V, INSPECT_PROFILE, INSPECT_PROFILE_RESET,
@@ -100,7 +101,8 @@ class Session:
     """One dflash_ctx on torch's current CUDA stream."""
 
     def __init__(self, w, max_batch: Optional[int] = None, max_seq_len: Optional[int] = None,
-                 keep_logits: bool = False, use_torch_alloc: bool = True, tensors: Optional[dict] = None):
+                 keep_logits: bool = False, use_torch_alloc: bool = True, tensors: Optional[dict] = None,
+                 graphs: bool = True):
         import torch
         if not torch.cuda.is_available():
             raise RuntimeError("no CUDA device: the dflash library has no CPU path")
@@ -110,6 +112,8 @@ class Session:
         self.max_batch = max_batch or w.batch
         self.max_seq_len = max_seq_len or (max(w.prompt_lens) + w.max_new_tokens + 3 * w.block_size + 8)
         self.cfg = config_from_workload(w, self.max_batch, self.max_seq_len, keep_logits)
+        if not graphs:
+            self.cfg.flags |= DFLASH_FLAG_NO_GRAPHS
         self.alloc = _TorchAllocator() if use_torch_alloc else None
         if self.alloc:
             self.cfg.alloc, self.cfg.free = self.alloc.alloc_cb, self.alloc.free_cb

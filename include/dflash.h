@@ -53,7 +53,8 @@ enum { DFLASH_DTYPE_F32 = 0, DFLASH_DTYPE_BF16 = 1 };
 /* Flags (dflash_config.flags). */
 enum {
     DFLASH_FLAG_KEEP_LOGITS = 1, /* keep fp32 logits of the last prefill / draft / verify for dflash_inspect */
-    DFLASH_FLAG_PROFILE = 2      /* time every kernel class with CUDA events (see DFLASH_INSPECT_PROFILE) */
+    DFLASH_FLAG_PROFILE = 2,     /* time every kernel class with CUDA events (see DFLASH_INSPECT_PROFILE) */
+    DFLASH_FLAG_NO_GRAPHS = 4    /* launch every kernel directly instead of replaying captured CUDA graphs */
 };
 
 /* Kernel classes reported by DFLASH_INSPECT_PROFILE. */
