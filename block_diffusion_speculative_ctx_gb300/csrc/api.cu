@@ -851,7 +851,13 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
         ALLOC(c->keep_verify, (size_t)rb * V * 4);
         ALLOC(c->keep_hidden, (size_t)rb * d * 4);
     }
-    if (cudaMemsetAsync(c->errw, 0, 16, c->stream) != cudaSuccess ||
+    // caches start at zero: attention stages whole 64-token pages, so slots past
+    // a sequence's length must hold finite values
+    if (cudaMemsetAsync(c->tK, 0, (size_t)c->Lt * c->kv.layer_stride * esz, c->stream) != cudaSuccess ||
+        cudaMemsetAsync(c->tV, 0, (size_t)c->Lt * c->kv.layer_stride * esz, c->stream) != cudaSuccess ||
+        cudaMemsetAsync(c->dK, 0, (size_t)c->Ld * c->kv.layer_stride * esz, c->stream) != cudaSuccess ||
+        cudaMemsetAsync(c->dV, 0, (size_t)c->Ld * c->kv.layer_stride * esz, c->stream) != cudaSuccess ||
+        cudaMemsetAsync(c->errw, 0, 16, c->stream) != cudaSuccess ||
         cudaMemsetAsync(c->gemm_counters, 0, (size_t)GEMM_COUNTERS * 4, c->stream) != cudaSuccess ||
         cudaMemsetAsync(c->n, 0, (size_t)cfg->max_batch * 4, c->stream) != cudaSuccess) {
         c->fail(DFLASH_E_CUDA, "memset failed");

@@ -1,4 +1,5 @@
-// Softmax attention over the paged KV cache for a group of query rows.
+// Softmax attention over the paged KV cache for a group of query rows
+// (CUDA-core kernel, used for fp32 storage; bf16 runs in attention_mma.cu).
 //
 // One CTA handles up to 64 query vectors = (rows of one sequence) x (the query
 // heads sharing one KV head), over one contiguous range of keys (a split).
@@ -269,16 +270,27 @@ void run(const Launch& L, const AttnParams& p) {
 
 }  // namespace
 
-template <typename T>
-void attention(const Launch& L, const AttnParams& p) {
+// fp32 storage: the CUDA-core kernel above.
+template <>
+void attention<float>(const Launch& L, const AttnParams& p) {
     if (p.rows <= 0) return;
     if (p.hd == 128)
-        run<T, 128>(L, p);
+        run<float, 128>(L, p);
     else
-        run<T, 64>(L, p);
+        run<float, 64>(L, p);
 }
 
-template void attention<float>(const Launch&, const AttnParams&);
-template void attention<bf16>(const Launch&, const AttnParams&);
+// bf16 storage: the tensor-core kernel (attention_mma.cu).
+template <>
+void attention<bf16>(const Launch& L, const AttnParams& p) {
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 148;
+    }
+    attention_mma(L, p, sms);
+}
 
 }  // namespace dfl

@@ -1,0 +1,399 @@
+// bf16 attention over the paged KV cache on the tensor cores (mma.sync
+// m16n8k16), for query blocks of one sequence: the draft block (bidirectional
+// over [context ; block], "DFlash: Block Diffusion for Flash Speculative
+// Decoding", Paper vs code "Attention pattern") and the verify block (causal).
+//
+// A CTA owns up to 64 query vectors (the block rows of one sequence times the
+// query heads sharing one KV head; four warps of 16) and one contiguous range
+// of 64-key tiles.  A key tile is exactly one cache page, so it is one
+// contiguous [64, head_dim] run in HBM; cp.async stages it (double-buffered)
+// into XOR-swizzled shared memory read by ldmatrix.  Scores are fp32; the
+// online softmax is fp32; P is split into bf16 hi + lo halves for the P.V
+// product so the result keeps ~fp32 accuracy.
+//
+// The key tiles of a query group are cut into S <= 8 ranges whose CTAs form a
+// thread-block cluster; each CTA parks (max, sum, unnormalised O) in shared
+// memory and, after a cluster barrier, CTA r merges query vectors
+// [r*64/S, (r+1)*64/S) over all ranks in rank order (deterministic), then
+// writes the bf16 output.  Every split range is derived on the device from the
+// sequence's current length, so the grid depends only on capacity.
+#include <math.h>
+
+#include "launch.h"
+
+namespace dfl {
+
+namespace {
+
+constexpr int KT = 64;      // keys per tile (= cache page)
+constexpr int NTHR = 128;   // 4 warps x 16 query vectors
+constexpr int QV = 64;
+
+__device__ __forceinline__ uint32_t s_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint32_t crank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void csync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(s_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+struct MmaArgs {
+    AttnParams p;
+    int g;        // query heads per KV head
+    int splits;   // cluster size
+    float scale_log2;  // log2(e) / sqrt(head_dim)
+};
+
+// Shared memory: K and V tiles, two stages each, rows of HD bf16 with the
+// 16-byte chunks of row r XOR-swizzled by (r & 7).
+template <int HD>
+struct AttnSmem {
+    static constexpr int TILE = KT * HD * 2;
+    static constexpr int KV_BYTES = 4 * TILE;                  // K[2], V[2]
+    static constexpr int PART = QV * HD * 4 + 2 * QV * 4;      // O, m, l (after the loop)
+    static constexpr int TOTAL = (KV_BYTES > PART ? KV_BYTES : PART) + 128;
+};
+
+template <int HD>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return (uint32_t)(row * (HD * 2) + ((chunk ^ (row & 7)) << 4));
+}
+
+template <int HD>
+__global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    using SM = AttnSmem<HD>;
+    constexpr int CH = HD / 8;         // 16-byte chunks per row
+    constexpr int NB_O = HD / 8;       // n-blocks of the output
+    extern __shared__ __align__(128) uint8_t sm[];
+    __shared__ int lim_s[QV];
+    __shared__ int glim_s;
+
+    const AttnParams& p = a.p;
+    const int grp = blockIdx.x, kvh = blockIdx.y;
+    const int S = a.splits;
+    const uint32_t rank = (S > 1) ? crank() : 0u;
+    const int g = a.g;
+    const int r0 = grp * p.group_rows;
+    const int nrows = min(p.group_rows, p.rows - r0);
+    const int nv = nrows * g;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seq = p.row_seq[r0];
+
+    if (tid == 0) glim_s = 0;
+    __syncthreads();
+    for (int v = tid; v < QV; v += NTHR) {
+        int lim = 0;
+        if (v < nv && seq >= 0) {
+            const int r = r0 + v / g;
+            if (p.row_seq[r] >= 0) lim = p.seq_len ? (p.seq_len[seq] + p.extra) : (p.row_pos[r] + 1);
+        }
+        lim_s[v] = lim;
+        atomicMax(&glim_s, lim);
+    }
+    __syncthreads();
+    const int glim = glim_s;
+    const int tiles = (glim + KT - 1) / KT;
+    const int per = (tiles + S - 1) / S;
+    const int t0 = (int)rank * per;
+    const int t1 = min(tiles, t0 + per);
+
+    const uint8_t* Kc = reinterpret_cast<const uint8_t*>(p.Kc);
+    const uint8_t* Vc = reinterpret_cast<const uint8_t*>(p.Vc);
+    uint8_t* Ks = sm;
+    uint8_t* Vs = sm + 2 * SM::TILE;
+
+    auto load_tile = [&](int t, int stage) {
+        // page of tile t holds keys [64 t, 64 t + 64) of this sequence
+        const int page = p.page_table[seq * p.kv.pages_per_seq + t];
+        const size_t off = ((size_t)page * p.kv.n_kv_heads + kvh) * (size_t)KT * HD * 2;
+        const uint8_t* ksrc = Kc + off;
+        const uint8_t* vsrc = Vc + off;
+        uint8_t* kd = Ks + stage * SM::TILE;
+        uint8_t* vd = Vs + stage * SM::TILE;
+        for (int i = tid; i < KT * CH; i += NTHR) {
+            const int r = i / CH, c = i % CH;
+            cp_async16(kd + swz<HD>(r, c), ksrc + (size_t)i * 16);
+            cp_async16(vd + swz<HD>(r, c), vsrc + (size_t)i * 16);
+        }
+        cp_commit();
+    };
+
+    // Q fragments (A operand), rows 16 warp + lane/4 (+8), head dims in k-steps of 16
+    const int qa = 16 * warp + (lane >> 2), qb = qa + 8;
+    uint32_t qf[HD / 16][4];
+    {
+        const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q);
+        auto qptr = [&](int v) -> const uint32_t* {
+            const int r = r0 + v / g, h = kvh * g + v % g;
+            return reinterpret_cast<const uint32_t*>(q + (size_t)r * p.H * HD + (size_t)h * HD);
+        };
+        const uint32_t* pa = qa < nv ? qptr(qa) : nullptr;
+        const uint32_t* pb = qb < nv ? qptr(qb) : nullptr;
+        const int c2 = lane & 3;  // column pair within 8
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+            qf[ks][0] = pa ? pa[ks * 8 + c2] : 0u;
+            qf[ks][1] = pb ? pb[ks * 8 + c2] : 0u;
+            qf[ks][2] = pa ? pa[ks * 8 + 4 + c2] : 0u;
+            qf[ks][3] = pb ? pb[ks * 8 + 4 + c2] : 0u;
+        }
+    }
+    const int lim_a = qa < nv ? lim_s[qa] : 0;
+    const int lim_b = qb < nv ? lim_s[qb] : 0;
+
+    float o[NB_O][4];
+#pragma unroll
+    for (int i = 0; i < NB_O; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+
+    if (t0 < t1) load_tile(t0, 0);
+    for (int t = t0; t < t1; ++t) {
+        const int stage = (t - t0) & 1;
+        if (t + 1 < t1) {
+            load_tile(t + 1, stage ^ 1);
+            cp_wait<1>();
+        } else {
+            cp_wait<0>();
+        }
+        __syncthreads();
+        const uint32_t kbase = s_u32(Ks + stage * SM::TILE);
+        const uint32_t vbase = s_u32(Vs + stage * SM::TILE);
+
+        // S = Q K^T for 64 keys: n-block nb covers keys 8 nb .. 8 nb + 7
+        float sc[8][4];
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+            sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+            const int krow = 8 * nb + (lane & 7);
+#pragma unroll
+            for (int kp = 0; kp < HD / 32; ++kp) {
+                // four 8x8 matrices: head-dim chunks 4 kp .. 4 kp + 3 of keys krow
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kbase + swz<HD>(krow, 4 * kp + (lane >> 3)), b0, b1, b2, b3);
+                mma_bf16(sc[nb], qf[2 * kp][0], qf[2 * kp][1], qf[2 * kp][2], qf[2 * kp][3], b0, b1);
+                mma_bf16(sc[nb], qf[2 * kp + 1][0], qf[2 * kp + 1][1], qf[2 * kp + 1][2], qf[2 * kp + 1][3], b2, b3);
+            }
+        }
+        // scale, mask, online softmax (base 2)
+        const int kbase_idx = t * KT + 2 * (lane & 3);
+        float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+            const int k0 = kbase_idx + 8 * nb;
+            sc[nb][0] = (k0 < lim_a) ? sc[nb][0] * a.scale_log2 : -INFINITY;
+            sc[nb][1] = (k0 + 1 < lim_a) ? sc[nb][1] * a.scale_log2 : -INFINITY;
+            sc[nb][2] = (k0 < lim_b) ? sc[nb][2] * a.scale_log2 : -INFINITY;
+            sc[nb][3] = (k0 + 1 < lim_b) ? sc[nb][3] * a.scale_log2 : -INFINITY;
+            mx_a = fmaxf(mx_a, fmaxf(sc[nb][0], sc[nb][1]));
+            mx_b = fmaxf(mx_b, fmaxf(sc[nb][2], sc[nb][3]));
+        }
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+        const float al_a = (mn_a == -INFINITY) ? 1.f : exp2f(m_a - mn_a);
+        const float al_b = (mn_b == -INFINITY) ? 1.f : exp2f(m_b - mn_b);
+        float sum_a = 0.f, sum_b = 0.f;
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+            sc[nb][0] = (sc[nb][0] == -INFINITY) ? 0.f : exp2f(sc[nb][0] - mn_a);
+            sc[nb][1] = (sc[nb][1] == -INFINITY) ? 0.f : exp2f(sc[nb][1] - mn_a);
+            sc[nb][2] = (sc[nb][2] == -INFINITY) ? 0.f : exp2f(sc[nb][2] - mn_b);
+            sc[nb][3] = (sc[nb][3] == -INFINITY) ? 0.f : exp2f(sc[nb][3] - mn_b);
+            sum_a += sc[nb][0] + sc[nb][1];
+            sum_b += sc[nb][2] + sc[nb][3];
+        }
+        sum_a += __shfl_xor_sync(0xffffffffu, sum_a, 1);
+        sum_a += __shfl_xor_sync(0xffffffffu, sum_a, 2);
+        sum_b += __shfl_xor_sync(0xffffffffu, sum_b, 1);
+        sum_b += __shfl_xor_sync(0xffffffffu, sum_b, 2);
+        l_a = l_a * al_a + sum_a;
+        l_b = l_b * al_b + sum_b;
+        m_a = mn_a;
+        m_b = mn_b;
+#pragma unroll
+        for (int i = 0; i < NB_O; ++i) {
+            o[i][0] *= al_a;
+            o[i][1] *= al_a;
+            o[i][2] *= al_b;
+            o[i][3] *= al_b;
+        }
+        // O += P V, P split into bf16 hi + lo; keys 16 kk .. 16 kk + 15 per k-step
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            uint32_t ph[4], pl[4];
+            {
+                const float* s0 = sc[2 * kk];
+                const float* s1 = sc[2 * kk + 1];
+                const float src[8] = {s0[0], s0[1], s0[2], s0[3], s1[0], s1[1], s1[2], s1[3]};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    ph[e] = pack_bf16(src[2 * e], src[2 * e + 1]);
+                    const float2 hv = unpack_bf16(ph[e]);
+                    pl[e] = pack_bf16(src[2 * e] - hv.x, src[2 * e + 1] - hv.y);
+                }
+            }
+            // A fragment order: (rows a, keys lo) (rows b, keys lo) (rows a, keys hi) (rows b, keys hi)
+            const uint32_t A0h = ph[0], A1h = ph[1], A2h = ph[2], A3h = ph[3];
+            const uint32_t A0l = pl[0], A1l = pl[1], A2l = pl[2], A3l = pl[3];
+            const int vrow = 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int hb = 0; hb < NB_O; hb += 2) {
+                // matrices: (keys 0-7, dims hb), (keys 8-15, dims hb), (keys 0-7, dims hb+1), (keys 8-15, dims hb+1)
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vbase + swz<HD>(vrow, hb + (lane >> 4)), b0, b1, b2, b3);
+                mma_bf16(o[hb], A0h, A1h, A2h, A3h, b0, b1);
+                mma_bf16(o[hb], A0l, A1l, A2l, A3l, b0, b1);
+                mma_bf16(o[hb + 1], A0h, A1h, A2h, A3h, b2, b3);
+                mma_bf16(o[hb + 1], A0l, A1l, A2l, A3l, b2, b3);
+            }
+        }
+        __syncthreads();  // the stage is overwritten by the next prefetch
+    }
+
+    // ---- merge the splits and write
+    float* Op = reinterpret_cast<float*>(sm);       // [QV][HD]
+    float* Mp = Op + QV * HD;                       // [QV]
+    float* Lp = Mp + QV;                            // [QV]
+    if (S > 1) {
+        // this thread's accumulators: rows qa / qb, dims 8 i + 2 (lane & 3) + {0, 1}
+#pragma unroll
+        for (int i = 0; i < NB_O; ++i) {
+            const int d = 8 * i + 2 * (lane & 3);
+            Op[qa * HD + d] = o[i][0];
+            Op[qa * HD + d + 1] = o[i][1];
+            Op[qb * HD + d] = o[i][2];
+            Op[qb * HD + d + 1] = o[i][3];
+        }
+        if ((lane & 3) == 0) {
+            Mp[qa] = m_a;
+            Lp[qa] = l_a;
+            Mp[qb] = m_b;
+            Lp[qb] = l_b;
+        }
+        csync();
+        const int vper = QV / S + ((QV % S) ? 1 : 0);
+        const int v0 = (int)rank * vper, v1 = min(QV, v0 + vper);
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+        for (int idx = tid; idx < (v1 - v0) * HD; idx += NTHR) {
+            const int v = v0 + idx / HD, d = idx % HD;
+            if (v >= nv) continue;
+            const int r = r0 + v / g, h = kvh * g + v % g;
+            if (p.row_seq[r] < 0) continue;
+            float mstar = -INFINITY;
+            float ms[8], ls[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (q < S) {
+                    ms[q] = ld_peer(Mp + v, (uint32_t)q);
+                    ls[q] = ld_peer(Lp + v, (uint32_t)q);
+                    mstar = fmaxf(mstar, ms[q]);
+                }
+            }
+            float num = 0.f, den = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (q < S && ms[q] != -INFINITY) {
+                    const float w = exp2f(ms[q] - mstar);
+                    num += w * ld_peer(Op + v * HD + d, (uint32_t)q);
+                    den += w * ls[q];
+                }
+            }
+            out[(size_t)r * p.H * HD + (size_t)h * HD + d] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+        }
+        csync();
+    } else {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+        const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
+        const bool wa = qa < nv && p.row_seq[r0 + qa / g] >= 0;
+        const bool wb = qb < nv && p.row_seq[r0 + qb / g] >= 0;
+        __nv_bfloat16* oa = wa ? out + (size_t)(r0 + qa / g) * p.H * HD + (size_t)(kvh * g + qa % g) * HD : nullptr;
+        __nv_bfloat16* ob = wb ? out + (size_t)(r0 + qb / g) * p.H * HD + (size_t)(kvh * g + qb % g) * HD : nullptr;
+#pragma unroll
+        for (int i = 0; i < NB_O; ++i) {
+            const int d = 8 * i + 2 * (lane & 3);
+            if (oa) *reinterpret_cast<__nv_bfloat162*>(oa + d) = __floats2bfloat162_rn(o[i][0] * ia, o[i][1] * ia);
+            if (ob) *reinterpret_cast<__nv_bfloat162*>(ob + d) = __floats2bfloat162_rn(o[i][2] * ib, o[i][3] * ib);
+        }
+    }
+}
+
+template <int HD>
+void run_mma(const Launch& L, const AttnParams& p, int sms) {
+    MmaArgs a;
+    a.p = p;
+    a.g = p.H / p.Hkv;
+    const int n_groups = (p.rows + p.group_rows - 1) / p.group_rows;
+    a.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+    // cluster size from the capacity (so the launch is the same every round)
+    const int cap_tiles = (p.max_keys + KT - 1) / KT;
+    const int base = n_groups * p.Hkv;
+    int S = 1;
+    while (S < 8 && S * 2 <= cap_tiles && base * S * 2 <= 2 * sms) S *= 2;
+    a.splits = S;
+    using SM = AttnSmem<HD>;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(attn_mma_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::TOTAL);
+        attr = true;
+    }
+    launch_k(L, attn_mma_kernel<HD>, dim3(n_groups, p.Hkv, S), dim3(NTHR), (size_t)SM::TOTAL, S, a);
+}
+
+}  // namespace
+
+// bf16 attention on mma.sync; the query group must hold at most 64 query vectors
+// (group_rows * H / H_kv <= 64) and the cache page must be 64 tokens.
+void attention_mma(const Launch& L, const AttnParams& p, int sms) {
+    if (p.rows <= 0) return;
+    if (p.hd == 128) run_mma<128>(L, p, sms);
+    else run_mma<64>(L, p, sms);
+}
+
+}  // namespace dfl

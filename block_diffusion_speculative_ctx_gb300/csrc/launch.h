@@ -137,6 +137,8 @@ struct AttnParams {
 };
 template <typename T>
 void attention(const Launch& L, const AttnParams& p);
+// bf16 path of attention(): tensor cores (mma.sync), cluster-merged key splits.
+void attention_mma(const Launch& L, const AttnParams& p, int sms);
 
 // ---- round bookkeeping
 // Block rows of a draft (proposal == nullptr) or verify pass: token of row
