@@ -86,6 +86,9 @@ struct dflash_ctx {
     void* stage = nullptr;
     float* fcout = nullptr;
     void* feat = nullptr;
+    float* ss_x = nullptr;   // [ss_tiles][R]: per-128-column sums of squares of x rows (fused norms)
+    float* ss_fc = nullptr;  // same for fcout
+    int ss_tiles = 0;
     float* kvout = nullptr;
     float* logits = nullptr;
     int* tokens = nullptr;
@@ -211,7 +214,8 @@ dflash_status validate(const dflash_config* c, std::string& why) {
     };
     if (c->dtype != DFLASH_DTYPE_F32 && c->dtype != DFLASH_DTYPE_BF16) return bad("dtype must be F32 or BF16");
     if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
-    if (c->d_model <= 0 || c->d_model % 64) return bad("d_model must be a positive multiple of 64");
+    if (c->d_model <= 0 || c->d_model % 64 || c->d_model > 8192)
+        return bad("d_model must be a positive multiple of 64, at most 8192");
     if (c->ffn <= 0 || c->ffn % 64) return bad("ffn must be a positive multiple of 64");
     if (c->n_heads <= 0 || c->n_kv_heads <= 0 || c->n_heads % c->n_kv_heads) return bad("n_heads % n_kv_heads != 0");
     if (c->n_heads / c->n_kv_heads > 64) return bad("more than 64 query heads per KV head");
@@ -272,8 +276,17 @@ dflash_status pack_layer(dflash_ctx* c, const dflash_layer_weights& w, LayerW& o
     if ((s = copy_rows(c, o.wqkv, qd, w.wk, kvd, d))) return s;
     if ((s = copy_rows(c, o.wqkv, qd + kvd, w.wv, kvd, d))) return s;
     if ((s = copy_rows(c, o.wo, 0, w.wo, d, qd))) return s;
-    if ((s = copy_rows(c, o.wgu, 0, w.w_gate, F, d))) return s;
-    if ((s = copy_rows(c, o.wgu, F, w.w_up, F, d))) return s;
+    if (c->cfg.dtype == DFLASH_DTYPE_BF16) {
+        // SwiGLU epilogue layout: tile j = gate rows [64j, 64j+64) then up rows [64j, 64j+64)
+        if (!w.w_gate || !w.w_up) return c->fail(DFLASH_E_INVAL, "a weight pointer is NULL");
+        const size_t blk = 64 * d * c->esz;
+        CUDA_TRY(c, cudaMemcpy2DAsync(o.wgu, 2 * blk, w.w_gate, blk, blk, F / 64, cudaMemcpyDeviceToDevice, c->stream));
+        CUDA_TRY(c, cudaMemcpy2DAsync((char*)o.wgu + blk, 2 * blk, w.w_up, blk, blk, F / 64, cudaMemcpyDeviceToDevice,
+                                      c->stream));
+    } else {
+        if ((s = copy_rows(c, o.wgu, 0, w.w_gate, F, d))) return s;
+        if ((s = copy_rows(c, o.wgu, F, w.w_up, F, d))) return s;
+    }
     if ((s = copy_rows(c, o.wdown, 0, w.w_down, d, F))) return s;
     if ((s = copy_norm(c, &o.attn_norm, w.attn_norm, d, false))) return s;
     if ((s = copy_norm(c, &o.mlp_norm, w.mlp_norm, d, false))) return s;
@@ -354,6 +367,63 @@ struct Pass {
 
     KVLayout kvl() const { return c->kv; }
 
+    static constexpr bool is_bf16 = sizeof(T) == 2;
+
+    // C (or the SwiGLU output `out`) = rms_norm(x, norm_w) . W^T for `rows` rows of the
+    // fp32 matrix x (row stride K).  bf16 blocks of <= 32 rows normalise inside the GEMM
+    // (sums of squares from ss_in, left there by the kernel that wrote x); otherwise an
+    // RMSNorm kernel writes the bf16/fp32 operand first.
+    void normed_gemm(int kind, int rows, const float* x, const float* norm_w, const float* ss_in, const T* W, int N,
+                     int K, float* C, int ldc, T* out, int ldo) {
+        Launch L = c->L();
+        const double R = rows, es = c->esz;
+        const double bytes = (double)N * K * es + R * K * 4 + (out ? R * ldo * es : R * N * 4.0);
+        const bool fused = is_bf16 && rows <= 32;
+        if (!fused)
+            timed(c, DFLASH_K_NORM, R * K * (4 + es), 0, [&] {
+                rmsnorm_rows<T>(L, x, K, norm_w, rows, K, c->cfg.rms_eps, (T*)c->xn, K);
+            });
+        timed(c, kind, bytes, 2 * R * N * (double)K, [&] {
+            if constexpr (sizeof(T) == 2) {
+                GemmEpi e;
+                if (fused) {
+                    e.x_f32 = x;
+                    e.ldx = K;
+                    e.norm_w = norm_w;
+                    e.ss_in = ss_in;
+                    e.ss_tiles = c->ss_tiles;
+                    e.ss_ld = c->R;
+                    e.eps = c->cfg.rms_eps;
+                }
+                if (out) {
+                    e.epi = 1;
+                    e.out = out;
+                    e.ldo = ldo;
+                }
+                if (!gemm_tc(L, (const bf16*)c->xn, K, rows, (const bf16*)W, rows, N, K, C, ldc, false, &e)) L.fail();
+            } else {
+                gemm<T>(L, (const T*)c->xn, K, W, rows, N, K, C, ldc, false);
+            }
+        });
+    }
+
+    // x += A . W^T (residual update); bf16 also leaves the sums of squares of the
+    // updated rows in ss_x for the next fused norm.
+    void residual_gemm(int kind, int rows, const T* A, int K, const T* W, int lda) {
+        Launch L = c->L();
+        const double R = rows, d = c->d;
+        timed(c, kind, gemm_bytes(c, R, d, K, true), 2 * R * d * (double)K, [&] {
+            if constexpr (sizeof(T) == 2) {
+                GemmEpi e;
+                e.ss_out = c->ss_x;
+                e.ss_ld = c->R;
+                if (!gemm_tc(L, (const bf16*)A, lda, rows, (const bf16*)W, rows, c->d, K, c->x, c->d, true, &e)) L.fail();
+            } else {
+                gemm<T>(L, A, lda, W, rows, c->d, K, c->x, c->d, true);
+            }
+        });
+    }
+
     // Decoder layers over `rows` rows whose metadata is (row_seq, row_pos).
     // target: causal attention over the target cache, capture of context layers
     // into stage; draft: bidirectional attention over [context ; block].
@@ -361,18 +431,13 @@ struct Pass {
                 bool capture, double keys_total) {
         Launch L = c->L();
         const int nl = target ? c->Lt : c->Ld;
-        T* xn = (T*)c->xn;
         const double R = rows, d = c->d, es = c->esz;
         for (int l = 0; l < nl; ++l) {
             const LayerW& w = target ? c->tl[l] : c->dl[l];
             void* Kc = elem<T>(target ? c->tK : c->dK, (size_t)l * c->kv.layer_stride);
             void* Vc = elem<T>(target ? c->tV : c->dV, (size_t)l * c->kv.layer_stride);
-            timed(c, DFLASH_K_NORM, R * d * (4 + es), 0, [&] {
-                rmsnorm_rows<T>(L, c->x, c->d, w.attn_norm, rows, c->d, c->cfg.rms_eps, xn, c->d);
-            });
-            timed(c, DFLASH_K_GEMM_QKV, gemm_bytes(c, R, c->qkv_n, d, false), 2 * R * c->qkv_n * d, [&] {
-                gemm<T>(L, xn, c->d, (const T*)w.wqkv, rows, c->qkv_n, c->d, c->qkv, c->qkv_n, false);
-            });
+            normed_gemm(DFLASH_K_GEMM_QKV, rows, c->x, w.attn_norm, c->ss_x, (const T*)w.wqkv, c->qkv_n, c->d,
+                        c->qkv, c->qkv_n, nullptr, 0);
             QKVStore st;
             st.qkv = c->qkv;
             st.ld = c->qkv_n;
@@ -418,19 +483,18 @@ struct Pass {
             ap.ws_bytes = ATTN_WS_BYTES;
             timed(c, DFLASH_K_ATTENTION, keys_total * 2 * c->kvd * es + 2 * R * c->qd * es,
                   4.0 * R * c->H * c->hd * (keys_total / std::max(1.0, (double)c->batch)), [&] { attention<T>(L, ap); });
-            timed(c, DFLASH_K_GEMM_O, gemm_bytes(c, R, d, c->qd, true), 2 * R * d * c->qd, [&] {
-                gemm<T>(L, (const T*)c->att, c->qd, (const T*)w.wo, rows, c->d, c->qd, c->x, c->d, true);
-            });
-            timed(c, DFLASH_K_NORM, R * d * (4 + es), 0, [&] {
-                rmsnorm_rows<T>(L, c->x, c->d, w.mlp_norm, rows, c->d, c->cfg.rms_eps, xn, c->d);
-            });
-            timed(c, DFLASH_K_GEMM_GATE_UP, gemm_bytes(c, R, 2.0 * c->F, d, false), 2 * R * 2.0 * c->F * d, [&] {
-                gemm<T>(L, xn, c->d, (const T*)w.wgu, rows, 2 * c->F, c->d, c->gu, 2 * c->F, false);
-            });
-            timed(c, DFLASH_K_SWIGLU, R * c->F * (8 + es), 0, [&] { silu_mul<T>(L, c->gu, c->F, rows, (T*)c->hmid); });
-            timed(c, DFLASH_K_GEMM_DOWN, gemm_bytes(c, R, d, c->F, true), 2 * R * d * c->F, [&] {
-                gemm<T>(L, (const T*)c->hmid, c->F, (const T*)w.wdown, rows, c->d, c->F, c->x, c->d, true);
-            });
+            residual_gemm(DFLASH_K_GEMM_O, rows, (const T*)c->att, c->qd, (const T*)w.wo, c->qd);
+            if (is_bf16) {
+                // gate/up GEMM with the fused norm and the SwiGLU epilogue -> hmid (bf16)
+                normed_gemm(DFLASH_K_GEMM_GATE_UP, rows, c->x, w.mlp_norm, c->ss_x, (const T*)w.wgu, 2 * c->F, c->d,
+                            nullptr, 0, (T*)c->hmid, c->F);
+            } else {
+                normed_gemm(DFLASH_K_GEMM_GATE_UP, rows, c->x, w.mlp_norm, c->ss_x, (const T*)w.wgu, 2 * c->F, c->d,
+                            c->gu, 2 * c->F, nullptr, 0);
+                timed(c, DFLASH_K_SWIGLU, R * c->F * (8 + es), 0,
+                      [&] { silu_mul<T>(L, c->gu, c->F, rows, (T*)c->hmid); });
+            }
+            residual_gemm(DFLASH_K_GEMM_DOWN, rows, (const T*)c->hmid, c->F, (const T*)w.wdown, c->F);
             if (target && capture && c->ctx_slot[l] >= 0)
                 timed(c, DFLASH_K_OTHER, R * d * (4 + es), 0, [&] {
                     capture_rows<T>(L, c->x, c->d, rows, (T*)c->stage, c->k * c->d, c->ctx_slot[l] * c->d);
@@ -444,17 +508,24 @@ struct Pass {
         Launch L = c->L();
         const double R = rows, d = c->d, es = c->esz;
         timed(c, DFLASH_K_GEMM_FC, gemm_bytes(c, R, d, c->k * d, false), 2 * R * d * c->k * d, [&] {
-            gemm<T>(L, (const T*)c->stage, c->k * c->d, (const T*)c->fc, rows, c->d, c->k * c->d, c->fcout, c->d, false);
-        });
-        timed(c, DFLASH_K_NORM, R * d * (4 + es), 0, [&] {
-            rmsnorm_rows<T>(L, c->fcout, c->d, c->fc_norm, rows, c->d, c->cfg.rms_eps, (T*)c->feat, c->d);
+            if (is_bf16) {
+                GemmEpi e;
+                e.ss_out = c->ss_fc;
+                e.ss_ld = c->R;
+                if (!gemm_tc(L, (const bf16*)c->stage, c->k * c->d, rows, (const bf16*)c->fc, rows, c->d, c->k * c->d,
+                             c->fcout, c->d, false, &e))
+                    L.fail();
+            } else {
+                gemm<T>(L, (const T*)c->stage, c->k * c->d, (const T*)c->fc, rows, c->d, c->k * c->d, c->fcout, c->d,
+                        false);
+            }
         });
         for (int l = 0; l < c->Ld; ++l) {
             const LayerW& w = c->dl[l];
             const T* wkv = elem<T>(w.wqkv, (size_t)c->qd * c->d);  // rows wk, wv
-            timed(c, DFLASH_K_GEMM_CTX_KV, gemm_bytes(c, R, 2.0 * c->kvd, d, false), 2 * R * 2.0 * c->kvd * d, [&] {
-                gemm<T>(L, (const T*)c->feat, c->d, wkv, rows, 2 * c->kvd, c->d, c->kvout, 2 * c->kvd, false);
-            });
+            // context feature rms(fcout) * fc_norm feeds every draft layer's K/V projection
+            normed_gemm(DFLASH_K_GEMM_CTX_KV, rows, c->fcout, c->fc_norm, c->ss_fc, wkv, 2 * c->kvd, c->d, c->kvout,
+                        2 * c->kvd, nullptr, 0);
             QKVStore st;
             st.qkv = c->kvout;
             st.ld = 2 * c->kvd;
@@ -486,12 +557,10 @@ struct Pass {
     void head(int row0, int rows, const float* norm, int* out, float* keep) {
         Launch L = c->L();
         const double R = rows, d = c->d, es = c->esz, V = c->V;
-        timed(c, DFLASH_K_NORM, R * d * (4 + es), 0, [&] {
-            rmsnorm_rows<T>(L, c->x + (size_t)row0 * c->d, c->d, norm, rows, c->d, c->cfg.rms_eps, (T*)c->xn, c->d);
-        });
-        timed(c, DFLASH_K_GEMM_HEAD, gemm_bytes(c, R, V, d, false), 2 * R * V * d, [&] {
-            gemm<T>(L, (const T*)c->xn, c->d, (const T*)c->head, rows, c->V, c->d, c->logits, c->V, false);
-        });
+        (void)d;
+        (void)es;
+        normed_gemm(DFLASH_K_GEMM_HEAD, rows, c->x + (size_t)row0 * c->d, norm, c->ss_x + row0, (const T*)c->head,
+                    c->V, c->d, c->logits, c->V, nullptr, 0);
         timed(c, DFLASH_K_ARGMAX, R * V * 4, 0, [&] { argmax_rows(L, c->logits, c->V, rows, c->V, out); });
         if (keep) cudaMemcpyAsync(keep, c->logits, (size_t)rows * c->V * 4, cudaMemcpyDeviceToDevice, c->stream);
     }
@@ -507,7 +576,7 @@ struct Pass {
                 CUDA_TRY(c, cudaMemcpyAsync(c->tokens, toks + off + r0, (size_t)rows * 4, cudaMemcpyHostToDevice,
                                             c->stream));
                 fill_prefill_rows(L, s, r0, rows, c->row_seq, c->row_pos);
-                embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, rows, c->x, c->errw);
+                embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, rows, c->x, c->errw, c->ss_x, c->R);
                 layers(true, rows, c->row_seq, c->row_pos, 64 / g, r0 + rows, true, (double)(r0 + rows));
                 append_context(rows, c->row_seq, c->row_pos);
                 if (r0 + rows == P)
@@ -535,7 +604,7 @@ struct Pass {
         timed(c, DFLASH_K_OTHER, (double)b * B * c->d * (4 + c->esz), 0, [&] {
             block_rows(L, b, B, c->n, c->anchor, nullptr, c->cfg.mask_token, c->V, c->max_seq, c->tokens, c->row_seq,
                        c->row_pos, c->errw);
-            embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, b * B, c->x, c->errw);
+            embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, b * B, c->x, c->errw, c->ss_x, c->R);
         });
         // attention grid sized from the session capacity, not the current length, so
         // that the pass is the same launch sequence every round (graph replay)
@@ -554,7 +623,7 @@ struct Pass {
         timed(c, DFLASH_K_OTHER, (double)b * B * c->d * (4 + c->esz), 0, [&] {
             block_rows(L, b, B, c->n, c->anchor, c->proposal, c->cfg.mask_token, c->V, c->max_seq, c->tokens,
                        c->row_seq, c->row_pos, c->errw);
-            embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, b * B, c->x, c->errw);
+            embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, b * B, c->x, c->errw, c->ss_x, c->R);
         });
         double keys = 0;
         for (int s = 0; s < b; ++s) keys += c->n_upper[s] + B;
@@ -825,6 +894,9 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     ALLOC(c->hmid, R * c->F * esz);
     ALLOC(c->stage, R * c->k * d * esz);
     ALLOC(c->fcout, R * d * 4);
+    c->ss_tiles = (c->d + 127) / 128;
+    ALLOC(c->ss_x, (size_t)c->ss_tiles * R * 4);
+    ALLOC(c->ss_fc, (size_t)c->ss_tiles * R * 4);
     ALLOC(c->feat, R * d * esz);
     ALLOC(c->kvout, R * 2 * c->kvd * 4);
     ALLOC(c->logits, (size_t)rb * V * 4);

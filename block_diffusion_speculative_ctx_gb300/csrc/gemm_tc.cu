@@ -30,6 +30,7 @@
 // in the error word, and the CTA still reaches its cluster barriers, releases
 // its TMEM and returns.
 #include <cuda.h>
+#include <string.h>
 
 #include <mutex>
 #include <unordered_map>
@@ -71,6 +72,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     }
     if (err) atomicOr(err, ERR_TIMEOUT);
     return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -184,21 +193,39 @@ struct TcArgs {
     int kb_per_split;
     int n_tiles;
     uint32_t* err;
+    // A operand normalised on the fly (NORM_A): bf16(x * rstd[m] * norm_w[k]), with
+    // rstd[m] = 1/sqrt(sum_t ss_in[t][m] / K + eps) from per-tile sums of squares
+    const float* norm_w;
+    const float* ss_in;
+    int ss_tiles, ss_ld;
+    float eps;
+    // epilogue: 0 = fp32 C (=|+=); 1 = SwiGLU, tile rows [0,64) gate and [64,128) up of
+    // features 64*tile + i, written as bf16 silu(gate) * up to out[m * ldo + f]
+    int epi;
+    void* out;
+    int ldo;
+    // epilogue 0: per-(tile, row) sum of squares of the final C values (or null)
+    float* ss_out;
 };
 
-template <int MT, int STAGES>
+template <int MT, int STAGES, bool NORM_A>
 struct Smem {
-    static constexpr int W_BYTES = BN * BK * 2;   // 16 KB
-    static constexpr int X_BYTES = MT * BK * 2;
-    static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+    static constexpr int W_BYTES = BN * BK * 2;             // 16 KB weight tile
+    static constexpr int X_BYTES = MT * BK * 2;             // bf16 activation tile (MMA operand)
+    static constexpr int XRAW_BYTES = NORM_A ? MT * BK * 4 : 0;  // fp32 residual tile (NORM_A)
+    static constexpr int STAGE_BYTES = W_BYTES + X_BYTES + XRAW_BYTES;
     static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-    static constexpr int TOTAL = BAR_OFF + (2 * STAGES + 1) * 8 + 16 + 1024;  // + alignment slack
+    static constexpr int NBAR = 2 * STAGES + 1 + (NORM_A ? 2 * STAGES : 0);
+    static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 64 * 4 + 1024;  // + rstd + alignment slack
 };
 
-template <int MT, int STAGES>
+// Sync of the four epilogue warps (warps 2..5) only.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int MT, int STAGES, bool NORM_A>
 __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                           const __grid_constant__ CUtensorMap tmX, TcArgs a) {
-    using S = Smem<MT, STAGES>;
+    using S = Smem<MT, STAGES, NORM_A>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles
     const uint32_t raw = smem_u32(smem_raw);
@@ -206,7 +233,10 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
     uint64_t* empty = full + STAGES;
     uint64_t* accf = empty + STAGES;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    uint64_t* xraw = accf + 1;          // NORM_A: raw fp32 tile landed
+    uint64_t* conv = xraw + STAGES;     // NORM_A: bf16 operand written by the epilogue warps
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::BAR_OFF + S::NBAR * 8);
+    float* rstd_s = reinterpret_cast<float*>(tmem_slot + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nt = blockIdx.x, mt = blockIdx.y, split = blockIdx.z;
@@ -223,6 +253,10 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            if (NORM_A) {
+                mbar_init(&xraw[s], 1);
+                mbar_init(&conv[s], 128);
+            }
         }
         mbar_init(accf, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -242,15 +276,23 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+            constexpr uint32_t FULL_TX = NORM_A ? S::W_BYTES : S::W_BYTES + S::X_BYTES;
             // weights of the first stages do not depend on the previous kernel
             const int pre = nkb < STAGES ? nkb : STAGES;
             for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], S::STAGE_BYTES);
+                mbar_arrive_expect_tx(&full[i], FULL_TX);
                 tma_load_2d(smem + i * S::STAGE_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0, pw);
             }
             pdl_wait();
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(smem + i * S::STAGE_BYTES + S::W_BYTES, &tmX, &full[i], (kb0 + i) * BK, m0, px);
+            for (int i = 0; i < pre; ++i) {
+                uint8_t* st = smem + i * S::STAGE_BYTES;
+                if (NORM_A) {
+                    mbar_arrive_expect_tx(&xraw[i], S::XRAW_BYTES);
+                    tma_load_2d(st + S::W_BYTES + S::X_BYTES, &tmX, &xraw[i], (kb0 + i) * BK, m0, px);
+                } else {
+                    tma_load_2d(st + S::W_BYTES, &tmX, &full[i], (kb0 + i) * BK, m0, px);
+                }
+            }
             for (int i = pre; i < nkb; ++i) {
                 const int s = i % STAGES;
                 if (!mbar_wait(&empty[s], ((i / STAGES) + 1) & 1, a.err)) {
@@ -258,10 +300,15 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
                     break;
                 }
                 uint8_t* st = smem + s * S::STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
                 const int kc = (kb0 + i) * BK;
+                mbar_arrive_expect_tx(&full[s], FULL_TX);
                 tma_load_2d(st, &tmW, &full[s], kc, n0, pw);
-                tma_load_2d(st + S::W_BYTES, &tmX, &full[s], kc, m0, px);
+                if (NORM_A) {
+                    mbar_arrive_expect_tx(&xraw[s], S::XRAW_BYTES);
+                    tma_load_2d(st + S::W_BYTES + S::X_BYTES, &tmX, &xraw[s], kc, m0, px);
+                } else {
+                    tma_load_2d(st + S::W_BYTES, &tmX, &full[s], kc, m0, px);
+                }
             }
         }
     } else if (warp == 1) {
@@ -270,6 +317,10 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % STAGES;
                 if (!mbar_wait(&full[s], (i / STAGES) & 1, a.err)) {
+                    ok = false;
+                    break;
+                }
+                if (NORM_A && !mbar_wait(&conv[s], (i / STAGES) & 1, a.err)) {
                     ok = false;
                     break;
                 }
@@ -284,6 +335,53 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
             }
             umma_commit(accf);  // fires once every MMA issued above has completed
         }
+    } else if (NORM_A) {
+        // epilogue warps convert each raw fp32 tile into the normalised bf16 operand
+        pdl_wait();
+        const int e = threadIdx.x - 64;  // 0..127
+        if (e < MT) {
+            float ss = 0.f;
+            const int m = m0 + e;
+            if (m < a.M)
+                for (int t = 0; t < a.ss_tiles; ++t) ss += a.ss_in[(size_t)t * a.ss_ld + m];
+            rstd_s[e] = rsqrtf(ss / (float)a.K + a.eps);
+        }
+        epi_sync();
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % STAGES;
+            uint8_t* st = smem + s * S::STAGE_BYTES;
+            if (!mbar_wait(&xraw[s], (i / STAGES) & 1, a.err)) ok = false;
+            const float* xr = reinterpret_cast<const float*>(st + S::W_BYTES + S::X_BYTES);
+            uint8_t* xb = st + S::W_BYTES;
+            const int kc = (kb0 + i) * BK;
+            // 16-byte output chunks: row m, k-chunk c (8 elements); swizzle chunk ^ (m & 7)
+            for (int ch = e; ch < MT * 8; ch += 128) {
+                const int m = ch >> 3, c = ch & 7;
+                const int k = kc + 8 * c;
+                const float4 x0 = *reinterpret_cast<const float4*>(xr + m * BK + 8 * c);
+                const float4 x1 = *reinterpret_cast<const float4*>(xr + m * BK + 8 * c + 4);
+                float w8[8];
+                if (k + 8 <= a.K) {
+                    const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.norm_w + k));
+                    const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.norm_w + k + 4));
+                    w8[0] = w0.x; w8[1] = w0.y; w8[2] = w0.z; w8[3] = w0.w;
+                    w8[4] = w1.x; w8[5] = w1.y; w8[6] = w1.z; w8[7] = w1.w;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) w8[j] = (k + j < a.K) ? a.norm_w[k + j] : 0.f;
+                }
+                const float r = rstd_s[m];
+                uint4 o;
+                o.x = pack2_bf16(x0.x * r * w8[0], x0.y * r * w8[1]);
+                o.y = pack2_bf16(x0.z * r * w8[2], x0.w * r * w8[3]);
+                o.z = pack2_bf16(x1.x * r * w8[4], x1.y * r * w8[5]);
+                o.w = pack2_bf16(x1.z * r * w8[6], x1.w * r * w8[7]);
+                *reinterpret_cast<uint4*>(xb + m * 128 + ((c ^ (m & 7)) << 4)) = o;
+            }
+            // generic-proxy writes must be visible to the tensor core's async proxy
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&conv[s]);
+        }
     }
     __syncwarp();
     pdl_wait();  // every thread: the previous kernel's outputs (C when accumulating) are visible
@@ -291,51 +389,78 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
     const int q = warp & 3;
     const int row = 32 * q + lane;  // feature within the tile
     const int n = n0 + row;
-    float* part = reinterpret_cast<float*>(smem);  // [MT][BN] partial tile (stage memory is free by then)
-    if (warp >= 2) {
-        // one lane waits; the warp then runs the .sync.aligned TMEM loads together
-        uint32_t okw = 0;
+    float* part = reinterpret_cast<float*>(smem);                  // [MT][BN] partial tile (cluster split-K)
+    float* xch = a.splits > 1 ? part + MT * BN : part;             // [MT][BN] final values (SwiGLU exchange)
+    float* ssw = xch + (a.epi == 1 ? MT * BN : 0);                 // [4][MT] per-warp sums of squares
+    const bool epi_warp = warp >= 2;
+    uint32_t okw = 0;
+    if (epi_warp) {
         if (lane == 0) okw = mbar_wait(accf, 0, a.err) ? 1u : 0u;
         ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
         tc_fence_after();
-        const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
-        float v[16];
-#pragma unroll
-        for (int c = 0; c < MT; c += 16) {
-            if (ok) tmem_ld16(tbase + c, v);
-            else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = 0.f;
+    }
+
+    // Final value of (token j, this row) -> C / SwiGLU exchange / sum of squares.
+    auto finish = [&](int j, float v, float* ss_acc) {
+        const int m = m0 + j;
+        if (a.epi == 0) {
+            float f = 0.f;
+            if (m < a.M && n < a.N) {
+                float* dst = a.C + (size_t)m * a.ldc + n;
+                f = a.accumulate ? (*dst + v) : v;
+                *dst = f;
             }
-            if (a.splits == 1) {
-                if (n < a.N) {
+            if (ss_acc) *ss_acc = f * f;
+        } else {
+            xch[j * BN + row] = v;
+        }
+    };
+
+    if (a.splits == 1) {
+        if (epi_warp) {
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
+            float v[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int m = m0 + c + j;
-                        if (m < a.M) {
-                            float* dst = a.C + (size_t)m * a.ldc + n;
-                            *dst = a.accumulate ? (*dst + v[j]) : v[j];
-                        }
+            for (int c = 0; c < MT; c += 16) {
+                if (ok) tmem_ld16(tbase + c, v);
+                else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float sq = 0.f;
+                    finish(c + j, v[j], a.ss_out ? &sq : nullptr);
+                    if (a.ss_out) {
+                        sq = warp_sum(sq);
+                        if (lane == 0) ssw[q * MT + c + j] = sq;
                     }
                 }
-            } else {
+            }
+        }
+    } else {
+        // ---- cluster split-K: rank r reduces its slice of columns over all ranks, in rank order
+        if (epi_warp) {
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
+            float v[16];
+#pragma unroll
+            for (int c = 0; c < MT; c += 16) {
+                if (ok) tmem_ld16(tbase + c, v);
+                else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) part[(c + j) * BN + row] = v[j];
             }
         }
-    }
-
-    if (a.splits > 1) {
-        // ---- cluster split-K: rank r reduces its slice of columns over all ranks, in rank order
         cluster_sync();
         const uint32_t rank = cluster_rank();
         const int per = (MT + a.splits - 1) / a.splits;
         const int j0 = (int)rank * per;
         const int j1 = min(MT, j0 + per);
-        if (warp >= 2 && n < a.N) {
+        if (epi_warp) {
             for (int j = j0; j < j1; ++j) {
-                const int m = m0 + j;
-                if (m >= a.M) break;
                 float vals[8];
 #pragma unroll
                 for (int r = 0; r < 8; ++r) vals[r] = (r < a.splits) ? ld_peer(part + j * BN + row, (uint32_t)r) : 0.f;
@@ -343,11 +468,43 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
 #pragma unroll
                 for (int r = 0; r < 8; ++r)
                     if (r < a.splits) acc += vals[r];
-                float* dst = a.C + (size_t)m * a.ldc + n;
-                *dst = a.accumulate ? (*dst + acc) : acc;
+                float sq = 0.f;
+                finish(j, acc, a.ss_out ? &sq : nullptr);
+                if (a.ss_out) {
+                    sq = warp_sum(sq);
+                    if (lane == 0) ssw[q * MT + j] = sq;
+                }
             }
         }
         cluster_sync();  // peers keep their shared memory until every slice is read
+    }
+
+    // ---- per-row sums of squares (epilogue 0) and SwiGLU (epilogue 1) need all 128 rows
+    if (epi_warp && (a.ss_out || a.epi == 1)) {
+        epi_sync();
+        int j0 = 0, j1 = MT;
+        if (a.splits > 1) {
+            const int per = (MT + a.splits - 1) / a.splits;
+            j0 = (int)cluster_rank() * per;
+            j1 = min(MT, j0 + per);
+        }
+        if (a.ss_out) {
+            const int e = threadIdx.x - 64;
+            if (e < j1 - j0) {
+                const int j = j0 + e, m = m0 + j;
+                if (m < a.M) a.ss_out[(size_t)nt * a.ss_ld + m] = ((ssw[j] + ssw[MT + j]) + ssw[2 * MT + j]) + ssw[3 * MT + j];
+            }
+        }
+        if (a.epi == 1 && row < 64) {
+            const int f = 64 * nt + row;  // feature index (gate row `row`, up row `row + 64`)
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+            for (int j = j0; j < j1; ++j) {
+                const int m = m0 + j;
+                if (m >= a.M || n0 + row >= a.N) continue;
+                const float gte = xch[j * BN + row], up = xch[j * BN + row + 64];
+                out[(size_t)m * a.ldo + f] = __float2bfloat16_rn(gte / (1.f + expf(-gte)) * up);
+            }
+        }
     }
 
     tc_fence_before();
@@ -380,26 +537,28 @@ EncodeTiledFn encode_fn() {
 struct MapKey {
     const void* ptr;
     long long rows, cols, ld;
-    int box_rows;
+    int box_rows, f32;
     bool operator==(const MapKey& o) const {
-        return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && box_rows == o.box_rows;
+        return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && box_rows == o.box_rows && f32 == o.f32;
     }
 };
 struct MapKeyHash {
     size_t operator()(const MapKey& k) const {
         size_t h = std::hash<const void*>()(k.ptr);
         h ^= std::hash<long long>()(k.rows * 1000003LL + k.cols) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
-        h ^= std::hash<long long>()(k.ld * 131 + k.box_rows) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+        h ^= std::hash<long long>()(k.ld * 131 + k.box_rows * 2 + k.f32) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
         return h;
     }
 };
 
-// Tensor map of a row-major bf16 matrix [rows, cols] (row stride ld elements),
-// box [box_rows, 64], 128-byte swizzle; out-of-range elements read as zero.
-bool make_map(CUtensorMap* out, const void* ptr, long long rows, long long cols, long long ld, int box_rows) {
+// Tensor map of a row-major matrix [rows, cols] (row stride ld elements), box
+// [box_rows, 64]: bf16 with 128-byte swizzle (MMA operands), or fp32 without
+// swizzle (raw residual tiles); out-of-range elements read as zero.
+bool make_map(CUtensorMap* out, const void* ptr, long long rows, long long cols, long long ld, int box_rows,
+              bool f32 = false) {
     static std::mutex mu;
     static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-    const MapKey key{ptr, rows, cols, ld, box_rows};
+    const MapKey key{ptr, rows, cols, ld, box_rows, f32 ? 1 : 0};
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) {
@@ -408,13 +567,15 @@ bool make_map(CUtensorMap* out, const void* ptr, long long rows, long long cols,
     }
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    const int esz = f32 ? 4 : 2;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
     cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUtensorMap m;
-    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    f32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     if (cache.size() > 65536) cache.clear();
@@ -454,25 +615,32 @@ int choose_splits(int tiles, int kb, int slots) {
     return best;
 }
 
-template <int MT, int STAGES>
+template <int MT, int STAGES, bool NORM_A>
 bool launch_tc(const Launch& L, const CUtensorMap& mw, const CUtensorMap& mx, TcArgs a, int m_tiles) {
-    using S = Smem<MT, STAGES>;
+    using S = Smem<MT, STAGES, NORM_A>;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(tc_gemm_kernel<MT, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(tc_gemm_kernel<MT, STAGES, NORM_A>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 S::TOTAL) != cudaSuccess)
             return false;
-        cudaFuncSetAttribute(tc_gemm_kernel<MT, STAGES>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        cudaFuncSetAttribute(tc_gemm_kernel<MT, STAGES, NORM_A>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
         attr = true;
     }
     const int KB = (a.K + BK - 1) / BK;
-    const int cta_per_sm = S::TOTAL <= 110 * 1024 ? 2 : 1;
-    const int splits = choose_splits(a.n_tiles * m_tiles, KB, sm_count() * cta_per_sm);
+    const int cta_per_sm = S::TOTAL <= 113 * 1024 ? 2 : 1;
+    int splits = choose_splits(a.n_tiles * m_tiles, KB, sm_count() * cta_per_sm);
+    // the epilogue reuses the stage memory: partials (split-K) + exchange (SwiGLU) + row sums
+    auto fits = [&](int sp) {
+        const size_t need = (sp > 1 ? (size_t)MT * BN * 4 : 0) + (a.epi == 1 ? (size_t)MT * BN * 4 : 0) + 16 * MT;
+        return need <= (size_t)STAGES * S::STAGE_BYTES;
+    };
+    if (!fits(splits)) splits = 1;
+    if (!fits(1)) return false;
     a.kb_per_split = (KB + splits - 1) / splits;
     a.splits = (KB + a.kb_per_split - 1) / a.kb_per_split;
     dim3 grid(a.n_tiles, m_tiles, a.splits);
-    launch_k(L, tc_gemm_kernel<MT, STAGES>, grid, dim3(THREADS), (size_t)S::TOTAL, a.splits, mw, mx, a);
+    launch_k(L, tc_gemm_kernel<MT, STAGES, NORM_A>, grid, dim3(THREADS), (size_t)S::TOTAL, a.splits, mw, mx, a);
     return true;
 }
 
@@ -481,17 +649,26 @@ bool launch_tc(const Launch& L, const CUtensorMap& mw, const CUtensorMap& mx, Tc
 // bf16 GEMM on the tensor cores.  Returns false when a tensor map cannot be
 // built (the caller reports the error); nothing is launched in that case.
 bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W, int M, int N, int K, float* C,
-             int ldc, bool accumulate) {
+             int ldc, bool accumulate, const GemmEpi* ep) {
+    static const GemmEpi none;
+    if (!ep) ep = &none;
+    const bool norm_a = ep->x_f32 != nullptr;
     int MT;
     if (M <= 16) MT = 16;
     else if (M <= 32) MT = 32;
     else if (M <= 64) MT = 64;
     else if (M <= 128) MT = 128;
     else MT = 256;
+    if (norm_a && MT > 32) return false;  // the fused norm serves blocks of at most 32 rows
     CUtensorMap mw, mx;
     if (!make_map(&mw, W, N, K, K, BN)) return false;
-    if (!make_map(&mx, A, a_rows, K, lda, MT)) return false;
+    if (norm_a) {
+        if (!make_map(&mx, ep->x_f32, a_rows, K, ep->ldx, MT, true)) return false;
+    } else if (!make_map(&mx, A, a_rows, K, lda, MT)) {
+        return false;
+    }
     TcArgs a;
+    memset(&a, 0, sizeof a);
     a.C = C;
     a.ldc = ldc;
     a.M = M;
@@ -501,14 +678,27 @@ bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W,
     a.n_tiles = (N + BN - 1) / BN;
     a.err = L.err;
     a.splits = 1;
-    a.kb_per_split = 0;
+    a.norm_w = ep->norm_w;
+    a.ss_in = ep->ss_in;
+    a.ss_tiles = ep->ss_tiles;
+    a.ss_ld = ep->ss_ld;
+    a.eps = ep->eps;
+    a.epi = ep->epi;
+    a.out = ep->out;
+    a.ldo = ep->ldo;
+    a.ss_out = ep->ss_out;
+    if (a.ss_out && a.epi != 0) return false;
     const int m_tiles = (M + MT - 1) / MT;
+    if (norm_a) {
+        if (MT == 16) return launch_tc<16, 4, true>(L, mw, mx, a, m_tiles);
+        return launch_tc<32, 3, true>(L, mw, mx, a, m_tiles);
+    }
     switch (MT) {
-        case 16: return launch_tc<16, 6>(L, mw, mx, a, m_tiles);
-        case 32: return launch_tc<32, 5>(L, mw, mx, a, m_tiles);
-        case 64: return launch_tc<64, 4>(L, mw, mx, a, m_tiles);
-        case 128: return launch_tc<128, 4>(L, mw, mx, a, m_tiles);
-        default: return launch_tc<256, 4>(L, mw, mx, a, m_tiles);
+        case 16: return launch_tc<16, 6, false>(L, mw, mx, a, m_tiles);
+        case 32: return launch_tc<32, 5, false>(L, mw, mx, a, m_tiles);
+        case 64: return launch_tc<64, 4, false>(L, mw, mx, a, m_tiles);
+        case 128: return launch_tc<128, 4, false>(L, mw, mx, a, m_tiles);
+        default: return launch_tc<256, 4, false>(L, mw, mx, a, m_tiles);
     }
 }
 

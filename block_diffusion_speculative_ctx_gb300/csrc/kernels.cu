@@ -8,9 +8,10 @@ namespace dfl {
 // ---------------------------------------------------------------- embedding
 template <typename T>
 __global__ void embed_kernel(const int* __restrict__ tokens, const T* __restrict__ embed, int vocab, int d,
-                             float* __restrict__ x, uint32_t* err) {
+                             float* __restrict__ x, uint32_t* err, float* __restrict__ ss_out, int ss_ld) {
     pdl_wait();
     pdl_trigger();
+    __shared__ float part[64][4];  // [128-column tile][quarter]
     const int r = blockIdx.x;
     int t = tokens[r];
     if (t < 0 || t >= vocab) {
@@ -19,14 +20,35 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const T* __restrict
     }
     const T* src = embed + (size_t)t * d;
     float* dst = x + (size_t)r * d;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) dst[c] = to_f32(src[c]);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // blockDim 256: in step i, warp w covers columns 256 i + 32 w .. +31, i.e. quarter (w & 3)
+    // of tile 2 i + (w >> 2); quarter sums are added in a fixed order below
+    for (int c0 = 0; c0 < d; c0 += 256) {
+        const int c = c0 + threadIdx.x;
+        float v = 0.f;
+        if (c < d) {
+            v = to_f32(src[c]);
+            dst[c] = v;
+        }
+        if (ss_out) {
+            const float sq = warp_sum(v * v);
+            if (lane == 0) part[(c0 >> 7) + (warp >> 2)][warp & 3] = sq;
+        }
+    }
+    if (ss_out) {
+        __syncthreads();
+        const int tiles = (d + 127) / 128;
+        if (threadIdx.x < tiles)
+            ss_out[(size_t)threadIdx.x * ss_ld + r] =
+                ((part[threadIdx.x][0] + part[threadIdx.x][1]) + part[threadIdx.x][2]) + part[threadIdx.x][3];
+    }
 }
 
 template <typename T>
 void embed_rows(const Launch& L, const int* tokens, const T* embed, int vocab, int d, int rows, float* x,
-                uint32_t* err) {
+                uint32_t* err, float* ss_out, int ss_ld) {
     if (rows <= 0) return;
-    launch_k(L, embed_kernel<T>, dim3(rows), dim3(256), 0, 1, tokens, embed, vocab, d, x, err);
+    launch_k(L, embed_kernel<T>, dim3(rows), dim3(256), 0, 1, tokens, embed, vocab, d, x, err, ss_out, ss_ld);
 }
 
 // ------------------------------------------------------------------ RMSNorm
@@ -292,7 +314,8 @@ void fill_prefill_rows(const Launch& L, int seq, int start_pos, int rows, int* r
 
 // ---- explicit instantiations
 #define DFL_INST(T)                                                                                         \
-    template void embed_rows<T>(const Launch&, const int*, const T*, int, int, int, float*, uint32_t*);     \
+    template void embed_rows<T>(const Launch&, const int*, const T*, int, int, int, float*, uint32_t*, float*, \
+                                int);                                                                       \
     template void rmsnorm_rows<T>(const Launch&, const float*, int, const float*, int, int, float, T*, int); \
     template void rmsnorm_gather<T>(const Launch&, const float*, int, const int*, const float*, int, int,   \
                                     float, T*, int);                                                        \

@@ -65,14 +65,40 @@ void launch_k(const Launch& L, void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 template <typename T>
 void gemm(const Launch& L, const T* A, int lda, const T* W, int M, int N, int K, float* C, int ldc, bool accumulate);
 
-// tcgen05 GEMM for bf16; false when it could not be launched (tensor map encode failed).
+// Options of the tcgen05 GEMM beyond C (=|+=) A.W^T:
+//  - x_f32 set: the A operand is the fp32 matrix x [M, K] (row stride ldx) normalised on
+//    the fly, A = bf16(x * rstd[m] * norm_w[k]) with rstd[m] = 1/sqrt(sum_t ss_in[t*ss_ld+m]/K + eps)
+//    (blocks of at most 32 rows); the A/lda arguments are ignored;
+//  - epi 1: SwiGLU; W holds, per 128-row tile j, gate rows [64j, 64j+64) then up rows
+//    [64j, 64j+64); out[m * ldo + f] = bf16(silu(gate_f) * up_f); C is unused;
+//  - ss_out set (epi 0): ss_out[tile * ss_ld + m] = sum over the tile's 128 columns of C[m][n]^2
+//    after the update, for the next fused norm.
+struct GemmEpi {
+    const float* x_f32 = nullptr;
+    int ldx = 0;
+    const float* norm_w = nullptr;
+    const float* ss_in = nullptr;
+    int ss_tiles = 0;
+    int ss_ld = 0;
+    float eps = 0.f;
+    int epi = 0;
+    void* out = nullptr;
+    int ldo = 0;
+    float* ss_out = nullptr;
+};
+
+// tcgen05 GEMM for bf16; false when it could not be launched (tensor map encode
+// failed or an unsupported option combination).
 bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W, int M, int N, int K, float* C,
-             int ldc, bool accumulate);
+             int ldc, bool accumulate, const GemmEpi* ep = nullptr);
 
 // ---- row kernels
+// Rows of the embedding table; with ss_out, also the per-128-column-tile sums of
+// squares of each row (ss_out[tile * ss_ld + row]) for the fused norm of the next GEMM.
+// d must be at most 64 * 128.
 template <typename T>
 void embed_rows(const Launch& L, const int* tokens, const T* embed, int vocab, int d, int rows, float* x,
-                uint32_t* err);
+                uint32_t* err, float* ss_out = nullptr, int ss_ld = 0);
 template <typename T>
 void rmsnorm_rows(const Launch& L, const float* x, int ldx, const float* w, int rows, int d, float eps, T* out,
                   int ldo);
