@@ -216,7 +216,7 @@ struct Smem {
     static constexpr int STAGE_BYTES = W_BYTES + X_BYTES + XRAW_BYTES;
     static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
     static constexpr int NBAR = 2 * STAGES + 1 + (NORM_A ? 2 * STAGES : 0);
-    static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 64 * 4 + 1024;  // + rstd + alignment slack
+    static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 64 * 4 + 128 * 4 + 1024;  // + rstd, partial sums, alignment
 };
 
 // Sync of the four epilogue warps (warps 2..5) only.
@@ -339,37 +339,60 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
         // epilogue warps convert each raw fp32 tile into the normalised bf16 operand
         pdl_wait();
         const int e = threadIdx.x - 64;  // 0..127
-        if (e < MT) {
-            float ss = 0.f;
-            const int m = m0 + e;
-            if (m < a.M)
-                for (int t = 0; t < a.ss_tiles; ++t) ss += a.ss_in[(size_t)t * a.ss_ld + m];
-            rstd_s[e] = rsqrtf(ss / (float)a.K + a.eps);
+        {
+            // rstd of the MT rows: thread (part, m) sums tiles part, part + P, ... (loads issued
+            // together), then the P part sums are added in a fixed order
+            constexpr int P = 128 / MT;
+            float* psum = rstd_s + 64;  // [P][MT]
+            const int m = e % MT, part = e / MT;
+            float acc = 0.f;
+            if (m0 + m < a.M) {
+                float v[8];
+                for (int t0 = part; t0 < a.ss_tiles; t0 += 8 * P) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int t = t0 + u * P;
+                        v[u] = t < a.ss_tiles ? __ldcg(a.ss_in + (size_t)t * a.ss_ld + m0 + m) : 0.f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) acc += v[u];
+                }
+            }
+            psum[part * MT + m] = acc;
+            epi_sync();
+            if (e < MT) {
+                float ss = 0.f;
+#pragma unroll
+                for (int p2 = 0; p2 < P; ++p2) ss += psum[p2 * MT + e];
+                rstd_s[e] = rsqrtf(ss / (float)a.K + a.eps);
+            }
+            epi_sync();
         }
-        epi_sync();
         for (int i = 0; i < nkb; ++i) {
             const int s = i % STAGES;
             uint8_t* st = smem + s * S::STAGE_BYTES;
+            const int kc = (kb0 + i) * BK;
+            // the norm weights of this stage load while the raw tile is in flight
+            const int c = e & 7;
+            const int k = kc + 8 * c;
+            float w8[8];
+            if (k + 8 <= a.K) {
+                const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.norm_w + k));
+                const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.norm_w + k + 4));
+                w8[0] = w0.x; w8[1] = w0.y; w8[2] = w0.z; w8[3] = w0.w;
+                w8[4] = w1.x; w8[5] = w1.y; w8[6] = w1.z; w8[7] = w1.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) w8[j] = (k + j < a.K) ? a.norm_w[k + j] : 0.f;
+            }
             if (!mbar_wait(&xraw[s], (i / STAGES) & 1, a.err)) ok = false;
             const float* xr = reinterpret_cast<const float*>(st + S::W_BYTES + S::X_BYTES);
             uint8_t* xb = st + S::W_BYTES;
-            const int kc = (kb0 + i) * BK;
             // 16-byte output chunks: row m, k-chunk c (8 elements); swizzle chunk ^ (m & 7)
             for (int ch = e; ch < MT * 8; ch += 128) {
-                const int m = ch >> 3, c = ch & 7;
-                const int k = kc + 8 * c;
+                const int m = ch >> 3;
                 const float4 x0 = *reinterpret_cast<const float4*>(xr + m * BK + 8 * c);
                 const float4 x1 = *reinterpret_cast<const float4*>(xr + m * BK + 8 * c + 4);
-                float w8[8];
-                if (k + 8 <= a.K) {
-                    const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.norm_w + k));
-                    const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.norm_w + k + 4));
-                    w8[0] = w0.x; w8[1] = w0.y; w8[2] = w0.z; w8[3] = w0.w;
-                    w8[4] = w1.x; w8[5] = w1.y; w8[6] = w1.z; w8[7] = w1.w;
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) w8[j] = (k + j < a.K) ? a.norm_w[k + j] : 0.f;
-                }
                 const float r = rstd_s[m];
                 uint4 o;
                 o.x = pack2_bf16(x0.x * r * w8[0], x0.y * r * w8[1]);
