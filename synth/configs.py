@@ -111,6 +111,9 @@ def _build() -> dict:
         weight_seed=7, prompt_seed=8)
     # Same model in fp32 storage (exact-token parity with a 128 head_dim and 16-wide blocks).
     w["small_f32"] = w["small_bf16"].with_(name="small_f32", dtype="f32")
+    # Prompt longer than one prefill chunk (2048 rows): chunked causal prefill.
+    w["small_bf16_long"] = w["small_bf16"].with_(name="small_bf16_long", prompt_lens=(2100, 300),
+                                                 prompt_seed=11)
     # LLaMA-style small model without target QK-norm, batch 4.
     w["small_bf16_llama"] = Workload(
         name="small_bf16_llama", dtype="bf16", vocab=3001, d_model=512, n_heads=4, n_kv_heads=1,

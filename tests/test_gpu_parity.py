@@ -148,6 +148,10 @@ def test_small_bf16_stepwise():
     assert run_stepwise("small_bf16", rounds=4) >= 4          # of 2 x 4
 
 
+def test_small_bf16_prompt_longer_than_a_prefill_chunk():
+    assert run_stepwise("small_bf16_long", rounds=3) >= 3     # of 2 x 3
+
+
 def test_small_bf16_llama_batch4_stepwise():
     assert run_stepwise("small_bf16_llama", rounds=4) >= 8    # of 4 x 4
 
