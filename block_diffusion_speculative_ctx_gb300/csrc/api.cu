@@ -101,6 +101,7 @@ struct dflash_ctx {
     int* proposal = nullptr;
     int* posterior = nullptr;
     int* argbuf = nullptr;
+    unsigned long long* keys = nullptr;  // head argmax keys [max_batch * B]
     int* accepted = nullptr;
     int* bonus = nullptr;
     int* drafts = nullptr;
@@ -374,7 +375,7 @@ struct Pass {
     // (sums of squares from ss_in, left there by the kernel that wrote x); otherwise an
     // RMSNorm kernel writes the bf16/fp32 operand first.
     void normed_gemm(int kind, int rows, const float* x, const float* norm_w, const float* ss_in, const T* W, int N,
-                     int K, float* C, int ldc, T* out, int ldo) {
+                     int K, float* C, int ldc, T* out, int ldo, unsigned long long* keys = nullptr) {
         Launch L = c->L();
         const double R = rows, es = c->esz;
         const double bytes = (double)N * K * es + R * K * 4 + (out ? R * ldo * es : R * N * 4.0);
@@ -399,6 +400,10 @@ struct Pass {
                     e.epi = 1;
                     e.out = out;
                     e.ldo = ldo;
+                }
+                if (keys) {
+                    e.epi = 2;
+                    e.keys = keys;
                 }
                 if (!gemm_tc(L, (const bf16*)c->xn, K, rows, (const bf16*)W, rows, N, K, C, ldc, false, &e)) L.fail();
             } else {
@@ -554,14 +559,27 @@ struct Pass {
     }
 
     // Final norm + shared head + row argmax over `rows` rows of x starting at row0.
-    void head(int row0, int rows, const float* norm, int* out, float* keep) {
+    // `block` > 0: draft rows, token ids of rows s*block+j (j >= 1) go to out[s*(block-1)+j-1].
+    void head(int row0, int rows, const float* norm, int* out, float* keep, int block = 0) {
         Launch L = c->L();
-        const double R = rows, d = c->d, es = c->esz, V = c->V;
-        (void)d;
-        (void)es;
-        normed_gemm(DFLASH_K_GEMM_HEAD, rows, c->x + (size_t)row0 * c->d, norm, c->ss_x + row0, (const T*)c->head,
-                    c->V, c->d, c->logits, c->V, nullptr, 0);
-        timed(c, DFLASH_K_ARGMAX, R * V * 4, 0, [&] { argmax_rows(L, c->logits, c->V, rows, c->V, out); });
+        const double R = rows, V = c->V;
+        if (is_bf16) {
+            // head GEMM with the argmax in its epilogue (logits written only when kept)
+            cudaMemsetAsync(c->keys, 0, (size_t)rows * sizeof(unsigned long long), c->stream);
+            normed_gemm(DFLASH_K_GEMM_HEAD, rows, c->x + (size_t)row0 * c->d, norm, c->ss_x + row0,
+                        (const T*)c->head, c->V, c->d, keep ? c->logits : nullptr, c->V, nullptr, 0, c->keys);
+            timed(c, DFLASH_K_ARGMAX, R * 8, 0, [&] { keys_to_ids(L, c->keys, rows, block, out); });
+        } else {
+            normed_gemm(DFLASH_K_GEMM_HEAD, rows, c->x + (size_t)row0 * c->d, norm, c->ss_x + row0,
+                        (const T*)c->head, c->V, c->d, c->logits, c->V, nullptr, 0);
+            if (block > 0) {
+                timed(c, DFLASH_K_ARGMAX, R * V * 4, 0, [&] { argmax_rows(L, c->logits, c->V, rows, c->V, c->argbuf); });
+                cudaMemcpy2DAsync(out, (size_t)(block - 1) * 4, c->argbuf + 1, (size_t)block * 4,
+                                  (size_t)(block - 1) * 4, rows / block, cudaMemcpyDeviceToDevice, c->stream);
+            } else {
+                timed(c, DFLASH_K_ARGMAX, R * V * 4, 0, [&] { argmax_rows(L, c->logits, c->V, rows, c->V, out); });
+            }
+        }
         if (keep) cudaMemcpyAsync(keep, c->logits, (size_t)rows * c->V * 4, cudaMemcpyDeviceToDevice, c->stream);
     }
 
@@ -611,10 +629,8 @@ struct Pass {
         double keys = 0;
         for (int s = 0; s < b; ++s) keys += c->n_upper[s] + B;
         layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, false, keys);
-        head(0, b * B, c->draft_norm, c->argbuf, c->keep_draft);
         // drafts[s][j] = argmax of row s*B + 1 + j
-        cudaMemcpy2DAsync(c->drafts, (size_t)(B - 1) * 4, c->argbuf + 1, (size_t)B * 4, (size_t)(B - 1) * 4, b,
-                          cudaMemcpyDeviceToDevice, c->stream);
+        head(0, b * B, c->draft_norm, c->drafts, c->keep_draft, B);
     }
 
     void verify() {
@@ -910,6 +926,7 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     ALLOC(c->proposal, (size_t)cfg->max_batch * c->B * 4);
     ALLOC(c->posterior, (size_t)rb * 4);
     ALLOC(c->argbuf, (size_t)rb * 4);
+    ALLOC(c->keys, (size_t)std::max(rb, cfg->max_batch) * 8);
     ALLOC(c->accepted, (size_t)cfg->max_batch * 4);
     ALLOC(c->bonus, (size_t)cfg->max_batch * 4);
     ALLOC(c->drafts, (size_t)cfg->max_batch * c->B * 4);

@@ -80,6 +80,17 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
     return v;
 }
 
+__device__ __forceinline__ float4 ld_peer4(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(s_u32(local)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
+
 struct MmaArgs {
     AttnParams p;
     int g;        // query heads per KV head
@@ -112,6 +123,7 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
     extern __shared__ __align__(128) uint8_t sm[];
     __shared__ int lim_s[QV];
     __shared__ int glim_s;
+    __shared__ float wsm[QV][8];  // split-merge weights of the query vectors this rank owns
 
     const AttnParams& p = a.p;
     const int grp = blockIdx.x, kvh = blockIdx.y;
@@ -306,10 +318,8 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
 #pragma unroll
         for (int i = 0; i < NB_O; ++i) {
             const int d = 8 * i + 2 * (lane & 3);
-            Op[qa * HD + d] = o[i][0];
-            Op[qa * HD + d + 1] = o[i][1];
-            Op[qb * HD + d] = o[i][2];
-            Op[qb * HD + d + 1] = o[i][3];
+            *reinterpret_cast<float2*>(Op + qa * HD + d) = make_float2(o[i][0], o[i][1]);
+            *reinterpret_cast<float2*>(Op + qb * HD + d) = make_float2(o[i][2], o[i][3]);
         }
         if ((lane & 3) == 0) {
             Mp[qa] = m_a;
@@ -320,32 +330,46 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
         csync();
         const int vper = QV / S + ((QV % S) ? 1 : 0);
         const int v0 = (int)rank * vper, v1 = min(QV, v0 + vper);
+        // combination weight of every rank for each query vector this rank owns
+        for (int v = v0 + tid; v < v1; v += NTHR) {
+            float ms[8], ls[8], mstar = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                ms[q] = q < S ? ld_peer(Mp + v, (uint32_t)q) : -INFINITY;
+                ls[q] = q < S ? ld_peer(Lp + v, (uint32_t)q) : 0.f;
+                mstar = fmaxf(mstar, ms[q]);
+            }
+            float den = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (ms[q] != -INFINITY) den += exp2f(ms[q] - mstar) * ls[q];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                wsm[v - v0][q] = (ms[q] != -INFINITY && den > 0.f) ? exp2f(ms[q] - mstar) / den : 0.f;
+        }
+        __syncthreads();
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-        for (int idx = tid; idx < (v1 - v0) * HD; idx += NTHR) {
-            const int v = v0 + idx / HD, d = idx % HD;
+        constexpr int C4 = HD / 4;
+        for (int idx = tid; idx < (v1 - v0) * C4; idx += NTHR) {
+            const int v = v0 + idx / C4, d = 4 * (idx % C4);
             if (v >= nv) continue;
             const int r = r0 + v / g, h = kvh * g + v % g;
             if (p.row_seq[r] < 0) continue;
-            float mstar = -INFINITY;
-            float ms[8], ls[8];
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                if (q < S) {
-                    ms[q] = ld_peer(Mp + v, (uint32_t)q);
-                    ls[q] = ld_peer(Lp + v, (uint32_t)q);
-                    mstar = fmaxf(mstar, ms[q]);
+                const float w = wsm[v - v0][q];
+                if (q < S && w != 0.f) {
+                    const float4 x = ld_peer4(Op + v * HD + d, (uint32_t)q);
+                    acc.x += w * x.x;
+                    acc.y += w * x.y;
+                    acc.z += w * x.z;
+                    acc.w += w * x.w;
                 }
             }
-            float num = 0.f, den = 0.f;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                if (q < S && ms[q] != -INFINITY) {
-                    const float w = exp2f(ms[q] - mstar);
-                    num += w * ld_peer(Op + v * HD + d, (uint32_t)q);
-                    den += w * ls[q];
-                }
-            }
-            out[(size_t)r * p.H * HD + (size_t)h * HD + d] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+            __nv_bfloat16* dst = out + (size_t)r * p.H * HD + (size_t)h * HD + d;
+            *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x, acc.y);
+            *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z, acc.w);
         }
         csync();
     } else {

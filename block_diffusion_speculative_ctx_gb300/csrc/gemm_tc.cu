@@ -206,6 +206,8 @@ struct TcArgs {
     int ldo;
     // epilogue 0: per-(tile, row) sum of squares of the final C values (or null)
     float* ss_out;
+    // epilogue 2 (argmax): keys[m] = max over n of argmax_key(C[m][n], n) (C also written when set)
+    unsigned long long* keys;
 };
 
 template <int MT, int STAGES, bool NORM_A>
@@ -415,6 +417,7 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
     float* part = reinterpret_cast<float*>(smem);                  // [MT][BN] partial tile (cluster split-K)
     float* xch = a.splits > 1 ? part + MT * BN : part;             // [MT][BN] final values (SwiGLU exchange)
     float* ssw = xch + (a.epi == 1 ? MT * BN : 0);                 // [4][MT] per-warp sums of squares
+    unsigned long long* wkey = reinterpret_cast<unsigned long long*>(ssw + 4 * MT);  // [4][MT] argmax keys
     const bool epi_warp = warp >= 2;
     uint32_t okw = 0;
     if (epi_warp) {
@@ -434,8 +437,20 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
                 *dst = f;
             }
             if (ss_acc) *ss_acc = f * f;
-        } else {
+        } else if (a.epi == 1) {
             xch[j * BN + row] = v;
+        } else {
+            unsigned long long key = 0ull;
+            if (m < a.M && n < a.N) {
+                if (a.C) a.C[(size_t)m * a.ldc + n] = v;
+                key = argmax_key(v, (uint32_t)n);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long t = __shfl_xor_sync(0xffffffffu, key, o);
+                key = t > key ? t : key;
+            }
+            if (lane == 0) wkey[q * MT + j] = key;
         }
     };
 
@@ -502,8 +517,8 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
         cluster_sync();  // peers keep their shared memory until every slice is read
     }
 
-    // ---- per-row sums of squares (epilogue 0) and SwiGLU (epilogue 1) need all 128 rows
-    if (epi_warp && (a.ss_out || a.epi == 1)) {
+    // ---- per-row sums of squares (epilogue 0), SwiGLU (1) and argmax (2) need all 128 rows
+    if (epi_warp && (a.ss_out || a.epi != 0)) {
         epi_sync();
         int j0 = 0, j1 = MT;
         if (a.splits > 1) {
@@ -516,6 +531,16 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
             if (e < j1 - j0) {
                 const int j = j0 + e, m = m0 + j;
                 if (m < a.M) a.ss_out[(size_t)nt * a.ss_ld + m] = ((ssw[j] + ssw[MT + j]) + ssw[2 * MT + j]) + ssw[3 * MT + j];
+            }
+        }
+        if (a.epi == 2) {
+            const int e = threadIdx.x - 64;
+            if (e < j1 - j0) {
+                const int j = j0 + e, m = m0 + j;
+                unsigned long long best = wkey[j];
+#pragma unroll
+                for (int w2 = 1; w2 < 4; ++w2) best = wkey[w2 * MT + j] > best ? wkey[w2 * MT + j] : best;
+                if (m < a.M) atomicMax(a.keys + m, best);
             }
         }
         if (a.epi == 1 && row < 64) {
@@ -655,7 +680,8 @@ bool launch_tc(const Launch& L, const CUtensorMap& mw, const CUtensorMap& mx, Tc
     int splits = choose_splits(a.n_tiles * m_tiles, KB, sm_count() * cta_per_sm);
     // the epilogue reuses the stage memory: partials (split-K) + exchange (SwiGLU) + row sums
     auto fits = [&](int sp) {
-        const size_t need = (sp > 1 ? (size_t)MT * BN * 4 : 0) + (a.epi == 1 ? (size_t)MT * BN * 4 : 0) + 16 * MT;
+        const size_t need = (sp > 1 ? (size_t)MT * BN * 4 : 0) + (a.epi == 1 ? (size_t)MT * BN * 4 : 0) + 16 * MT +
+                            32 * MT;
         return need <= (size_t)STAGES * S::STAGE_BYTES;
     };
     if (!fits(splits)) splits = 1;
@@ -710,7 +736,9 @@ bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W,
     a.out = ep->out;
     a.ldo = ep->ldo;
     a.ss_out = ep->ss_out;
+    a.keys = ep->keys;
     if (a.ss_out && a.epi != 0) return false;
+    if (a.epi == 2 && !a.keys) return false;
     const int m_tiles = (M + MT - 1) / MT;
     if (norm_a) {
         if (MT == 16) return launch_tc<16, 4, true>(L, mw, mx, a, m_tiles);

@@ -236,6 +236,26 @@ void argmax_rows(const Launch& L, const float* logits, long long ld, int rows, i
     launch_k(L, argmax_kernel, dim3(rows), dim3(1024), 0, 1, logits, ld, V, out);
 }
 
+__global__ void keys_to_ids_kernel(const unsigned long long* __restrict__ keys, int rows, int block,
+                                   int* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows) return;
+    const int id = (int)argmax_key_index(keys[r]);
+    if (block <= 0) {
+        out[r] = id;
+    } else {
+        const int j = r % block;
+        if (j) out[(r / block) * (block - 1) + j - 1] = id;
+    }
+}
+
+void keys_to_ids(const Launch& L, const unsigned long long* keys, int rows, int block, int* out) {
+    if (rows <= 0) return;
+    launch_k(L, keys_to_ids_kernel, dim3((rows + 127) / 128), dim3(128), 0, 1, keys, rows, block, out);
+}
+
 // --------------------------------------------------------- round bookkeeping
 __global__ void block_rows_kernel(int batch, int B, const int* __restrict__ n, const int* __restrict__ anchor,
                                   const int* __restrict__ proposal, int mask, int vocab, int max_pos,

@@ -72,7 +72,9 @@ void gemm(const Launch& L, const T* A, int lda, const T* W, int M, int N, int K,
 //  - epi 1: SwiGLU; W holds, per 128-row tile j, gate rows [64j, 64j+64) then up rows
 //    [64j, 64j+64); out[m * ldo + f] = bf16(silu(gate_f) * up_f); C is unused;
 //  - ss_out set (epi 0): ss_out[tile * ss_ld + m] = sum over the tile's 128 columns of C[m][n]^2
-//    after the update, for the next fused norm.
+//    after the update, for the next fused norm;
+//  - epi 2: row argmax: keys[m] = max_n argmax_key(C[m][n], n) by atomicMax (keys start at zero; C is
+//    still written when non-null).
 struct GemmEpi {
     const float* x_f32 = nullptr;
     int ldx = 0;
@@ -85,6 +87,7 @@ struct GemmEpi {
     void* out = nullptr;
     int ldo = 0;
     float* ss_out = nullptr;
+    unsigned long long* keys = nullptr;  // epi 2: per-row argmax keys (zeroed by the caller)
 };
 
 // tcgen05 GEMM for bf16; false when it could not be launched (tensor map encode
@@ -138,6 +141,10 @@ void silu_mul(const Launch& L, const float* gu, int F, int rows, T* out);
 // (context-layer capture): stage[r * ld_stage + col + c] = x[r * d + c].
 template <typename T>
 void capture_rows(const Launch& L, const float* x, int d, int rows, T* stage, int ld_stage, int col);
+
+// Token ids from argmax keys: out[r] = index(keys[r]); with block > 0 (draft rows), only rows
+// r with r % block != 0 are written, to out[(r / block) * (block - 1) + r % block - 1].
+void keys_to_ids(const Launch& L, const unsigned long long* keys, int rows, int block, int* out);
 
 // Row argmax over logits [rows, V] (row stride ld); lowest index wins on ties.
 void argmax_rows(const Launch& L, const float* logits, long long ld, int rows, int V, int* out);
