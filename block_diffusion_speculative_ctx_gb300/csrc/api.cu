@@ -375,7 +375,8 @@ struct Pass {
     // (sums of squares from ss_in, left there by the kernel that wrote x); otherwise an
     // RMSNorm kernel writes the bf16/fp32 operand first.
     void normed_gemm(int kind, int rows, const float* x, const float* norm_w, const float* ss_in, const T* W, int N,
-                     int K, float* C, int ldc, T* out, int ldo, unsigned long long* keys = nullptr) {
+                     int K, float* C, int ldc, T* out, int ldo, unsigned long long* keys = nullptr,
+                     const QkvStoreEpi* qkv = nullptr) {
         Launch L = c->L();
         const double R = rows, es = c->esz;
         const double bytes = (double)N * K * es + R * K * 4 + (out ? R * ldo * es : R * N * 4.0);
@@ -405,11 +406,36 @@ struct Pass {
                     e.epi = 2;
                     e.keys = keys;
                 }
+                e.qkv = qkv;
                 if (!gemm_tc(L, (const bf16*)c->xn, K, rows, (const bf16*)W, rows, N, K, C, ldc, false, &e)) L.fail();
             } else {
                 gemm<T>(L, (const T*)c->xn, K, W, rows, N, K, C, ldc, false);
             }
         });
+    }
+
+    // q/k norm, RoPE and the cache store run in the projection GEMM's epilogue for
+    // bf16 blocks of <= 32 rows with head_dim 128 (one head per 128-row weight tile).
+    bool qkv_in_epilogue(int rows) const { return is_bf16 && rows <= 32 && c->hd == 128; }
+
+    QkvStoreEpi qkv_epi(int q_heads, const float* q_norm, const float* k_norm, void* Kc, void* Vc,
+                        const int* row_seq, const int* row_pos) const {
+        QkvStoreEpi e;
+        e.q_heads = q_heads;
+        e.kv_heads = c->Hkv;
+        e.hd = c->hd;
+        e.q_norm = q_norm;
+        e.k_norm = k_norm;
+        e.rope = reinterpret_cast<const float2*>(c->rope);
+        e.max_pos = c->max_seq;
+        e.q_out = c->q;
+        e.Kc = Kc;
+        e.Vc = Vc;
+        e.kv = c->kv;
+        e.page_table = c->page_table;
+        e.row_seq = row_seq;
+        e.row_pos = row_pos;
+        return e;
     }
 
     // x += A . W^T (residual update); bf16 also leaves the sums of squares of the
@@ -441,8 +467,10 @@ struct Pass {
             const LayerW& w = target ? c->tl[l] : c->dl[l];
             void* Kc = elem<T>(target ? c->tK : c->dK, (size_t)l * c->kv.layer_stride);
             void* Vc = elem<T>(target ? c->tV : c->dV, (size_t)l * c->kv.layer_stride);
+            const bool fuse_qkv = qkv_in_epilogue(rows);
+            const QkvStoreEpi qe = qkv_epi(c->H, w.q_norm, w.k_norm, Kc, Vc, row_seq, row_pos);
             normed_gemm(DFLASH_K_GEMM_QKV, rows, c->x, w.attn_norm, c->ss_x, (const T*)w.wqkv, c->qkv_n, c->d,
-                        c->qkv, c->qkv_n, nullptr, 0);
+                        c->qkv, c->qkv_n, nullptr, 0, nullptr, fuse_qkv ? &qe : nullptr);
             QKVStore st;
             st.qkv = c->qkv;
             st.ld = c->qkv_n;
@@ -466,7 +494,8 @@ struct Pass {
             st.page_table = c->page_table;
             st.rows = rows;
             st.err = c->errw;
-            timed(c, DFLASH_K_ROPE_STORE, R * c->qkv_n * (4 + es), 0, [&] { qk_norm_rope_store<T>(L, st); });
+            if (!fuse_qkv)
+                timed(c, DFLASH_K_ROPE_STORE, R * c->qkv_n * (4 + es), 0, [&] { qk_norm_rope_store<T>(L, st); });
             AttnParams ap;
             ap.q = c->q;
             ap.Kc = Kc;
@@ -529,8 +558,11 @@ struct Pass {
             const LayerW& w = c->dl[l];
             const T* wkv = elem<T>(w.wqkv, (size_t)c->qd * c->d);  // rows wk, wv
             // context feature rms(fcout) * fc_norm feeds every draft layer's K/V projection
+            const bool fuse_kv = qkv_in_epilogue(rows);
+            const QkvStoreEpi qe = qkv_epi(0, nullptr, w.k_norm, elem<T>(c->dK, (size_t)l * c->kv.layer_stride),
+                                           elem<T>(c->dV, (size_t)l * c->kv.layer_stride), ctx_seq, ctx_pos);
             normed_gemm(DFLASH_K_GEMM_CTX_KV, rows, c->fcout, c->fc_norm, c->ss_fc, wkv, 2 * c->kvd, c->d, c->kvout,
-                        2 * c->kvd, nullptr, 0);
+                        2 * c->kvd, nullptr, 0, nullptr, fuse_kv ? &qe : nullptr);
             QKVStore st;
             st.qkv = c->kvout;
             st.ld = 2 * c->kvd;
@@ -554,7 +586,8 @@ struct Pass {
             st.page_table = c->page_table;
             st.rows = rows;
             st.err = c->errw;
-            timed(c, DFLASH_K_ROPE_STORE, R * 2.0 * c->kvd * (4 + es), 0, [&] { qk_norm_rope_store<T>(L, st); });
+            if (!fuse_kv)
+                timed(c, DFLASH_K_ROPE_STORE, R * 2.0 * c->kvd * (4 + es), 0, [&] { qk_norm_rope_store<T>(L, st); });
         }
     }
 

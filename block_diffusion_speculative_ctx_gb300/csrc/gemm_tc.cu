@@ -168,6 +168,21 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+struct QkvEpi {
+    int q_tiles, n_kv;
+    const float* q_norm;
+    const float* k_norm;
+    const float2* rope;  // [max_pos][64]
+    int max_pos;
+    __nv_bfloat16* q_out;
+    __nv_bfloat16* Kc;
+    __nv_bfloat16* Vc;
+    KVLayout kv;
+    const int* page_table;
+    const int* row_seq;
+    const int* row_pos;
+};
+
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -208,6 +223,11 @@ struct TcArgs {
     float* ss_out;
     // epilogue 2 (argmax): keys[m] = max over n of argmax_key(C[m][n], n) (C also written when set)
     unsigned long long* keys;
+    // epilogue 3 (q/k/v of head_dim 128: one head per tile): tiles [0, q_tiles) are query heads,
+    // then n_kv key heads, then n_kv value heads; per-head RMSNorm of q (q_norm) and k (k_norm),
+    // RoPE at row_pos[m], q to q_out [M, q_tiles*128], k and v into the paged cache at
+    // (row_seq[m], row_pos[m]); rows with row_seq < 0 are skipped
+    QkvEpi qkv;
 };
 
 template <int MT, int STAGES, bool NORM_A>
@@ -223,6 +243,25 @@ struct Smem {
 
 // Sync of the four epilogue warps (warps 2..5) only.
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Reduce 16 per-token values over the 32 lanes of a warp (v[t] = this lane's value of
+// token t) with 16 shuffles: each halving step keeps one half of the tokens and sends
+// the other half to the partner lane.  On return every lane holds the reduction of
+// token (lane >> 1).
+template <typename T, typename Op>
+__device__ __forceinline__ T transpose_reduce16(T (&v)[16], int lane, Op op) {
+#pragma unroll
+    for (int o = 16, c = 16; o >= 2; o >>= 1, c >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < c / 2; ++i) {
+            const T send = upper ? v[i] : v[i + c / 2];
+            const T keep = upper ? v[i + c / 2] : v[i];
+            v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, o));
+        }
+    }
+    return op(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+}
 
 template <int MT, int STAGES, bool NORM_A>
 __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
@@ -416,7 +455,7 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
     const int n = n0 + row;
     float* part = reinterpret_cast<float*>(smem);                  // [MT][BN] partial tile (cluster split-K)
     float* xch = a.splits > 1 ? part + MT * BN : part;             // [MT][BN] final values (SwiGLU exchange)
-    float* ssw = xch + (a.epi == 1 ? MT * BN : 0);                 // [4][MT] per-warp sums of squares
+    float* ssw = xch + ((a.epi == 1 || a.epi == 3) ? MT * BN : 0);  // [4][MT] per-warp sums of squares
     unsigned long long* wkey = reinterpret_cast<unsigned long long*>(ssw + 4 * MT);  // [4][MT] argmax keys
     const bool epi_warp = warp >= 2;
     uint32_t okw = 0;
@@ -426,23 +465,34 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
         tc_fence_after();
     }
 
-    // Final value of (token j, this row) -> C / SwiGLU exchange / sum of squares.
-    auto finish = [&](int j, float v, float* ss_acc) {
-        const int m = m0 + j;
-        if (a.epi == 0) {
+    // Kernel arguments used per token, hoisted into registers once.
+    const int epi = a.epi;
+    float* const Cp = a.C;
+    const size_t ldc = (size_t)a.ldc;
+    const bool accum = a.accumulate != 0;
+    const bool has_ss = a.ss_out != nullptr;
+    const bool n_ok = n < a.N;
+    const int m_left = a.M - m0;  // tokens j < m_left of this tile are real rows
+
+    // Final value of (token j, this row) -> C / exchange tile / sum of squares / argmax key.
+    auto finish = [=](int j, float v) {
+        if (epi == 0) {
             float f = 0.f;
-            if (m < a.M && n < a.N) {
-                float* dst = a.C + (size_t)m * a.ldc + n;
-                f = a.accumulate ? (*dst + v) : v;
+            if (n_ok && j < m_left) {
+                float* dst = Cp + (size_t)(m0 + j) * ldc + n;
+                f = accum ? (*dst + v) : v;
                 *dst = f;
             }
-            if (ss_acc) *ss_acc = f * f;
-        } else if (a.epi == 1) {
+            if (has_ss) {
+                const float sq = warp_sum(f * f);
+                if (lane == 0) ssw[q * MT + j] = sq;
+            }
+        } else if (epi == 1 || epi == 3) {
             xch[j * BN + row] = v;
         } else {
             unsigned long long key = 0ull;
-            if (m < a.M && n < a.N) {
-                if (a.C) a.C[(size_t)m * a.ldc + n] = v;
+            if (n_ok && j < m_left) {
+                if (Cp) Cp[(size_t)(m0 + j) * ldc + n] = v;
                 key = argmax_key(v, (uint32_t)n);
             }
 #pragma unroll
@@ -458,21 +508,60 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
         if (epi_warp) {
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
             float v[16];
-#pragma unroll
+            // Groups of 16 accumulator columns, kept rolled (an unrolled loop would hold
+            // MT copies of the epilogue code); one specialised loop per epilogue kind.
+#pragma unroll 1
             for (int c = 0; c < MT; c += 16) {
                 if (ok) tmem_ld16(tbase + c, v);
                 else {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) v[j] = 0.f;
                 }
+                if (epi == 0 && !has_ss) {
+                    float* dst = Cp + (size_t)(m0 + c) * ldc + n;
+                    const int lim = n_ok ? min(16, m_left - c) : 0;
+                    if (accum) {
+                        float old[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    float sq = 0.f;
-                    finish(c + j, v[j], a.ss_out ? &sq : nullptr);
-                    if (a.ss_out) {
-                        sq = warp_sum(sq);
-                        if (lane == 0) ssw[q * MT + c + j] = sq;
+                        for (int j = 0; j < 16; ++j) old[j] = j < lim ? dst[j * ldc] : 0.f;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (j < lim) dst[j * ldc] = old[j] + v[j];
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (j < lim) dst[j * ldc] = v[j];
                     }
+                } else if (epi == 0) {
+                    // C update plus the per-token sum of squares over the tile's 128 rows
+                    float* dst = Cp + (size_t)(m0 + c) * ldc + n;
+                    const int lim = n_ok ? min(16, m_left - c) : 0;
+                    float f[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) f[j] = (accum && j < lim) ? dst[j * ldc] : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        f[j] = j < lim ? f[j] + v[j] : 0.f;
+                        if (j < lim) dst[j * ldc] = f[j];
+                        f[j] *= f[j];
+                    }
+                    const float sq = transpose_reduce16(f, lane, [](float x, float y) { return x + y; });
+                    if (!(lane & 1)) ssw[q * MT + c + (lane >> 1)] = sq;
+                } else if (epi == 1 || epi == 3) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) xch[(c + j) * BN + row] = v[j];
+                } else {
+                    // row argmax keys: the best (value, index) of each token over the tile's rows
+                    const int lim = n_ok ? min(16, m_left - c) : 0;
+                    unsigned long long k[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        k[j] = j < lim ? argmax_key(v[j], (uint32_t)n) : 0ull;
+                        if (Cp && j < lim) Cp[(size_t)(m0 + c + j) * ldc + n] = v[j];
+                    }
+                    const unsigned long long best = transpose_reduce16(
+                        k, lane, [](unsigned long long x, unsigned long long y) { return x > y ? x : y; });
+                    if (!(lane & 1)) wkey[q * MT + c + (lane >> 1)] = best;
                 }
             }
         }
@@ -481,8 +570,8 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
         if (epi_warp) {
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
             float v[16];
-#pragma unroll
-            for (int c = 0; c < MT; c += 16) {
+#pragma unroll 1
+            for (int c = 0; c < MT; c += 16) {  // rolled: an unrolled body is MT copies of the epilogue code
                 if (ok) tmem_ld16(tbase + c, v);
                 else {
 #pragma unroll
@@ -506,12 +595,7 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
 #pragma unroll
                 for (int r = 0; r < 8; ++r)
                     if (r < a.splits) acc += vals[r];
-                float sq = 0.f;
-                finish(j, acc, a.ss_out ? &sq : nullptr);
-                if (a.ss_out) {
-                    sq = warp_sum(sq);
-                    if (lane == 0) ssw[q * MT + j] = sq;
-                }
+                finish(j, acc);
             }
         }
         cluster_sync();  // peers keep their shared memory until every slice is read
@@ -526,16 +610,15 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
             j0 = (int)cluster_rank() * per;
             j1 = min(MT, j0 + per);
         }
+        // one token per epilogue thread, 128 at a time (tiles of 256 tokens take two passes)
         if (a.ss_out) {
-            const int e = threadIdx.x - 64;
-            if (e < j1 - j0) {
+            for (int e = threadIdx.x - 64; e < j1 - j0; e += 128) {
                 const int j = j0 + e, m = m0 + j;
                 if (m < a.M) a.ss_out[(size_t)nt * a.ss_ld + m] = ((ssw[j] + ssw[MT + j]) + ssw[2 * MT + j]) + ssw[3 * MT + j];
             }
         }
         if (a.epi == 2) {
-            const int e = threadIdx.x - 64;
-            if (e < j1 - j0) {
+            for (int e = threadIdx.x - 64; e < j1 - j0; e += 128) {
                 const int j = j0 + e, m = m0 + j;
                 unsigned long long best = wkey[j];
 #pragma unroll
@@ -543,14 +626,63 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
                 if (m < a.M) atomicMax(a.keys + m, best);
             }
         }
-        if (a.epi == 1 && row < 64) {
-            const int f = 64 * nt + row;  // feature index (gate row `row`, up row `row + 64`)
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+        if (a.epi == 3) {
+            const QkvEpi& Q = a.qkv;
+            const int kind = nt < Q.q_tiles ? 0 : (nt < Q.q_tiles + Q.n_kv ? 1 : 2);  // q / k / v head
+            const int head = kind == 0 ? nt : (kind == 1 ? nt - Q.q_tiles : nt - Q.q_tiles - Q.n_kv);
+            const float* nw = kind == 0 ? Q.q_norm : (kind == 1 ? Q.k_norm : nullptr);
+            if (nw) {
+                // per-head RMSNorm over the tile's 128 rows (each thread rescales only its own row)
+                for (int j = j0; j < j1; ++j) {
+                    const float x = xch[j * BN + row];
+                    const float sq = warp_sum(x * x);
+                    if (lane == 0) ssw[q * MT + j] = sq;
+                }
+                epi_sync();
+                const float w = nw[row];
+                for (int j = j0; j < j1; ++j) {
+                    const float ss = ((ssw[j] + ssw[MT + j]) + ssw[2 * MT + j]) + ssw[3 * MT + j];
+                    xch[j * BN + row] = xch[j * BN + row] * rsqrtf(ss / (float)BN + a.eps) * w;
+                }
+            }
+            if (kind < 2) epi_sync();  // RoPE reads the partner row
             for (int j = j0; j < j1; ++j) {
                 const int m = m0 + j;
-                if (m >= a.M || n0 + row >= a.N) continue;
-                const float gte = xch[j * BN + row], up = xch[j * BN + row + 64];
-                out[(size_t)m * a.ldo + f] = __float2bfloat16_rn(gte / (1.f + expf(-gte)) * up);
+                if (m >= a.M) break;
+                const int seq = Q.row_seq[m], pos = Q.row_pos[m];
+                if (seq < 0) continue;
+                if (pos < 0 || pos >= Q.max_pos) {
+                    if (row == 0 && a.err) atomicOr(a.err, ERR_POSITION_RANGE);
+                    continue;
+                }
+                float val = xch[j * BN + row];
+                if (kind < 2) {
+                    const float partner = xch[j * BN + (row ^ 64)];
+                    const float2 cs = Q.rope[(size_t)pos * 64 + (row & 63)];
+                    val = row < 64 ? val * cs.x - partner * cs.y : val * cs.x + partner * cs.y;
+                }
+                const __nv_bfloat16 o = __float2bfloat16_rn(val);
+                if (kind == 0) {
+                    Q.q_out[(size_t)m * Q.q_tiles * BN + (size_t)head * BN + row] = o;
+                } else {
+                    __nv_bfloat16* base = kind == 1 ? Q.Kc : Q.Vc;
+                    base[kv_offset(Q.kv, Q.page_table, seq, pos, head) + row] = o;
+                }
+            }
+        }
+        if (a.epi == 1) {
+            // thread e: feature r = e % 64 (gate row r, up row r + 64) of tokens j0 + e / 64, +2, ...
+            const int e = threadIdx.x - 64;
+            const int r = e & 63;
+            const int f = 64 * nt + r;
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+            if (n0 + r < a.N) {
+                for (int j = j0 + (e >> 6); j < j1; j += 2) {
+                    const int m = m0 + j;
+                    if (m >= a.M) break;
+                    const float gte = xch[j * BN + r], up = xch[j * BN + r + 64];
+                    out[(size_t)m * a.ldo + f] = __float2bfloat16_rn(gte / (1.f + expf(-gte)) * up);
+                }
             }
         }
     }
@@ -643,24 +775,18 @@ int sm_count() {
     return n;
 }
 
-// Split count (cluster size, <= 8) that best fills `slots` concurrent CTAs
-// while keeping at least four K blocks per split.
-int choose_splits(int tiles, int kb, int slots) {
-    int best = 1;
-    double best_eff = 0.0;
-    for (int s = 1; s <= 8; ++s) {
-        if (s > 1 && kb / s < 4) break;
-        const int kbps = (kb + s - 1) / s;
-        const int real = (kb + kbps - 1) / kbps;
-        const long long ctas = (long long)tiles * real;
-        const long long waves = (ctas + slots - 1) / slots;
-        const double eff = (double)ctas / (double)(waves * slots);
-        if (eff > best_eff + 0.03) {
-            best_eff = eff;
-            best = s;
-        }
-    }
-    return best;
+// Split count (cluster size): the largest power of two that keeps the grid within
+// one wave of `slots` CTAs.  The cluster reduction of the [MT x 128] fp32 partial
+// tile grows with MT, so wider tiles split less: up to 8 ways for tiles of <= 32
+// tokens (>= 4 K blocks per split), 4 ways for 64 (>= 4) and 128 (>= 48 K blocks
+// per split, i.e. long K only), never for 256.
+int choose_splits(int tiles, int kb, int slots, int mt) {
+    if (mt >= 256) return 1;
+    const int cap = mt <= 32 ? 8 : 4;
+    const int min_kb = mt <= 64 ? 4 : 48;
+    int s = 1;
+    while (s < cap && (long long)tiles * (2 * s) <= slots && kb / (2 * s) >= min_kb) s *= 2;
+    return s;
 }
 
 template <int MT, int STAGES, bool NORM_A>
@@ -677,11 +803,11 @@ bool launch_tc(const Launch& L, const CUtensorMap& mw, const CUtensorMap& mx, Tc
     }
     const int KB = (a.K + BK - 1) / BK;
     const int cta_per_sm = S::TOTAL <= 113 * 1024 ? 2 : 1;
-    int splits = choose_splits(a.n_tiles * m_tiles, KB, sm_count() * cta_per_sm);
+    int splits = choose_splits(a.n_tiles * m_tiles, KB, sm_count() * cta_per_sm, MT);
     // the epilogue reuses the stage memory: partials (split-K) + exchange (SwiGLU) + row sums
     auto fits = [&](int sp) {
-        const size_t need = (sp > 1 ? (size_t)MT * BN * 4 : 0) + (a.epi == 1 ? (size_t)MT * BN * 4 : 0) + 16 * MT +
-                            32 * MT;
+        const size_t need = (sp > 1 ? (size_t)MT * BN * 4 : 0) +
+                            ((a.epi == 1 || a.epi == 3) ? (size_t)MT * BN * 4 : 0) + 16 * MT + 32 * MT;
         return need <= (size_t)STAGES * S::STAGE_BYTES;
     };
     if (!fits(splits)) splits = 1;
@@ -737,6 +863,25 @@ bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W,
     a.ldo = ep->ldo;
     a.ss_out = ep->ss_out;
     a.keys = ep->keys;
+    if (ep->qkv) {
+        const QkvStoreEpi& src = *ep->qkv;
+        if (src.hd != BN || a.epi != 0) return false;
+        a.epi = 3;
+        a.qkv.q_tiles = src.q_heads;
+        a.qkv.n_kv = src.kv_heads;
+        a.qkv.q_norm = src.q_norm;
+        a.qkv.k_norm = src.k_norm;
+        a.qkv.rope = src.rope;
+        a.qkv.max_pos = src.max_pos;
+        a.qkv.q_out = reinterpret_cast<__nv_bfloat16*>(src.q_out);
+        a.qkv.Kc = reinterpret_cast<__nv_bfloat16*>(src.Kc);
+        a.qkv.Vc = reinterpret_cast<__nv_bfloat16*>(src.Vc);
+        a.qkv.kv = src.kv;
+        a.qkv.page_table = src.page_table;
+        a.qkv.row_seq = src.row_seq;
+        a.qkv.row_pos = src.row_pos;
+        if (N != (src.q_heads + 2 * src.kv_heads) * BN) return false;
+    }
     if (a.ss_out && a.epi != 0) return false;
     if (a.epi == 2 && !a.keys) return false;
     const int m_tiles = (M + MT - 1) / MT;

@@ -75,6 +75,23 @@ void gemm(const Launch& L, const T* A, int lda, const T* W, int M, int N, int K,
 //    after the update, for the next fused norm;
 //  - epi 2: row argmax: keys[m] = max_n argmax_key(C[m][n], n) by atomicMax (keys start at zero; C is
 //    still written when non-null).
+// q/k/v epilogue of the tcgen05 GEMM (head_dim 128): the GEMM's N columns are q_heads
+// query heads, then kv_heads key heads, then kv_heads value heads (q_heads may be 0).
+struct QkvStoreEpi {
+    int q_heads, kv_heads, hd;
+    const float* q_norm;   // [hd] or nullptr
+    const float* k_norm;   // [hd] or nullptr
+    const float2* rope;    // [max_pos][hd/2]
+    int max_pos;
+    void* q_out;           // bf16 [M, q_heads * hd]
+    void* Kc;              // cache layer base (bf16)
+    void* Vc;
+    KVLayout kv;
+    const int* page_table;
+    const int* row_seq;    // [M]; < 0 = skip
+    const int* row_pos;
+};
+
 struct GemmEpi {
     const float* x_f32 = nullptr;
     int ldx = 0;
@@ -88,6 +105,7 @@ struct GemmEpi {
     int ldo = 0;
     float* ss_out = nullptr;
     unsigned long long* keys = nullptr;  // epi 2: per-row argmax keys (zeroed by the caller)
+    const QkvStoreEpi* qkv = nullptr;    // epi 3: norm + RoPE + store of q/k/v heads (C unused)
 };
 
 // tcgen05 GEMM for bf16; false when it could not be launched (tensor map encode

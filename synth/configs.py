@@ -120,6 +120,11 @@ def _build() -> dict:
         head_dim=128, ffn=1408, target_layers=5, target_qk_norm=False, rope_theta=5e5, draft_layers=3,
         block_size=16, ctx_layer_ids=(1, 2, 3), batch=4, prompt_lens=(64, 5, 130, 33), max_new_tokens=40,
         norm_std=0.1, weight_seed=9, prompt_seed=10)
+    # Same shapes at batch 12: draft and verify passes of 192 rows (256-token GEMM tiles);
+    # weight std 0.04 keeps most greedy choices clear of bf16 near-ties.
+    w["small_bf16_llama_b12"] = w["small_bf16_llama"].with_(
+        name="small_bf16_llama_b12", batch=12, prompt_lens=(64, 5, 130, 33, 17, 90, 41, 8, 120, 77, 3, 50),
+        weight_std=0.04, prompt_seed=12)
     return w
 
 

@@ -156,6 +156,11 @@ def test_small_bf16_llama_batch4_stepwise():
     assert run_stepwise("small_bf16_llama", rounds=4) >= 8    # of 4 x 4
 
 
+def test_small_bf16_llama_batch12_stepwise():
+    # 192 block rows per pass: GEMM tiles of 256 tokens, tokens 128..191 in the tile's second half
+    assert run_stepwise("small_bf16_llama_b12", rounds=3) >= 18    # of 12 x 3
+
+
 def test_block_size_one_is_plain_greedy():
     assert run_stepwise("tiny_f32_b3", rounds=5, block_size=1) == 3 * 5
 
