@@ -459,7 +459,7 @@ struct Pass {
     // target: causal attention over the target cache, capture of context layers
     // into stage; draft: bidirectional attention over [context ; block].
     void layers(bool target, int rows, const int* row_seq, const int* row_pos, int group_rows, int max_keys,
-                bool capture, double keys_total) {
+                bool capture, double keys_total, int rows_per_seq = 0) {
         Launch L = c->L();
         const int nl = target ? c->Lt : c->Ld;
         const double R = rows, d = c->d, es = c->esz;
@@ -508,6 +508,7 @@ struct Pass {
             ap.extra = target ? 0 : c->B;
             ap.rows = rows;
             ap.group_rows = group_rows;
+            ap.seq_div = rows_per_seq;
             ap.H = c->H;
             ap.Hkv = c->Hkv;
             ap.hd = c->hd;
@@ -661,7 +662,7 @@ struct Pass {
         // that the pass is the same launch sequence every round (graph replay)
         double keys = 0;
         for (int s = 0; s < b; ++s) keys += c->n_upper[s] + B;
-        layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, false, keys);
+        layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, false, keys, B);
         // drafts[s][j] = argmax of row s*B + 1 + j
         head(0, b * B, c->draft_norm, c->drafts, c->keep_draft, B);
     }
@@ -676,7 +677,7 @@ struct Pass {
         });
         double keys = 0;
         for (int s = 0; s < b; ++s) keys += c->n_upper[s] + B;
-        layers(true, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, true, keys);
+        layers(true, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, true, keys, B);
         if (c->keep_hidden)
             cudaMemcpyAsync(c->keep_hidden, c->x, (size_t)b * B * c->d * 4, cudaMemcpyDeviceToDevice, c->stream);
         head(0, b * B, c->final_norm, c->posterior, c->keep_verify);

@@ -11,12 +11,14 @@
 // online softmax is fp32; P is split into bf16 hi + lo halves for the P.V
 // product so the result keeps ~fp32 accuracy.
 //
-// The key tiles of a query group are cut into S <= 8 ranges whose CTAs form a
-// thread-block cluster; each CTA parks (max, sum, unnormalised O) in shared
-// memory and, after a cluster barrier, CTA r merges query vectors
-// [r*64/S, (r+1)*64/S) over all ranks in rank order (deterministic), then
-// writes the bf16 output.  Every split range is derived on the device from the
-// sequence's current length, so the grid depends only on capacity.
+// The key tiles of a query group are dealt round-robin to S <= 16 CTAs that form
+// a thread-block cluster (rank r takes tiles r, r + S, ...): the first page of
+// every rank is known before the sequence length is read, so its K/V load
+// starts one memory round trip earlier.  Each CTA parks (max, sum, unnormalised
+// O) in shared memory and, after a cluster barrier, CTA r merges its share of
+// the 64 query vectors over all ranks in rank order (deterministic), then writes
+// the bf16 output.  The tiles a rank takes follow from the sequence's current
+// length on the device, so the grid depends only on capacity.
 #include <math.h>
 
 #include "launch.h"
@@ -28,6 +30,7 @@ namespace {
 constexpr int KT = 64;      // keys per tile (= cache page)
 constexpr int NTHR = 128;   // 4 warps x 16 query vectors
 constexpr int QV = 64;
+constexpr int SMAX = 16;    // largest cluster (non-portable above 8)
 
 __device__ __forceinline__ uint32_t s_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -60,9 +63,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
-}
 
 __device__ __forceinline__ uint32_t crank() {
     uint32_t r;
@@ -94,7 +94,7 @@ __device__ __forceinline__ float4 ld_peer4(const float* local, uint32_t rank) {
 struct MmaArgs {
     AttnParams p;
     int g;        // query heads per KV head
-    int splits;   // cluster size
+    int splits;   // cluster size (<= SMAX)
     float scale_log2;  // log2(e) / sqrt(head_dim)
 };
 
@@ -123,7 +123,6 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
     extern __shared__ __align__(128) uint8_t sm[];
     __shared__ int lim_s[QV];
     __shared__ int glim_s;
-    __shared__ float wsm[QV][8];  // split-merge weights of the query vectors this rank owns
 
     const AttnParams& p = a.p;
     const int grp = blockIdx.x, kvh = blockIdx.y;
@@ -134,25 +133,8 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
     const int nrows = min(p.group_rows, p.rows - r0);
     const int nv = nrows * g;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int seq = p.row_seq[r0];
-
-    if (tid == 0) glim_s = 0;
-    __syncthreads();
-    for (int v = tid; v < QV; v += NTHR) {
-        int lim = 0;
-        if (v < nv && seq >= 0) {
-            const int r = r0 + v / g;
-            if (p.row_seq[r] >= 0) lim = p.seq_len ? (p.seq_len[seq] + p.extra) : (p.row_pos[r] + 1);
-        }
-        lim_s[v] = lim;
-        atomicMax(&glim_s, lim);
-    }
-    __syncthreads();
-    const int glim = glim_s;
-    const int tiles = (glim + KT - 1) / KT;
-    const int per = (tiles + S - 1) / S;
-    const int t0 = (int)rank * per;
-    const int t1 = min(tiles, t0 + per);
+    // sequence of this group: from the row layout when it is sequence-major, else from row_seq
+    const int seq = p.seq_div > 0 ? r0 / p.seq_div : p.row_seq[r0];
 
     const uint8_t* Kc = reinterpret_cast<const uint8_t*>(p.Kc);
     const uint8_t* Vc = reinterpret_cast<const uint8_t*>(p.Vc);
@@ -174,6 +156,25 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
         }
         cp_commit();
     };
+    // this rank's first tile (index `rank`, inside the sequence's page range) loads while
+    // the key limits are read; it is dropped below if the sequence is shorter
+    const bool early = seq >= 0 && (int)rank < p.kv.pages_per_seq;
+    if (early) load_tile((int)rank, 0);
+
+    if (tid == 0) glim_s = 0;
+    __syncthreads();
+    for (int v = tid; v < QV; v += NTHR) {
+        int lim = 0;
+        if (v < nv && seq >= 0) {
+            const int r = r0 + v / g;
+            if (p.row_seq[r] >= 0) lim = p.seq_len ? (p.seq_len[seq] + p.extra) : (p.row_pos[r] + 1);
+        }
+        lim_s[v] = lim;
+        atomicMax(&glim_s, lim);
+    }
+    __syncthreads();
+    const int glim = glim_s;
+    const int tiles = (glim + KT - 1) / KT;
 
     // Q fragments (A operand), rows 16 warp + lane/4 (+8), head dims in k-steps of 16
     const int qa = 16 * warp + (lane >> 2), qb = qa + 8;
@@ -203,11 +204,12 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
     for (int i = 0; i < NB_O; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
 
-    if (t0 < t1) load_tile(t0, 0);
-    for (int t = t0; t < t1; ++t) {
-        const int stage = (t - t0) & 1;
-        if (t + 1 < t1) {
-            load_tile(t + 1, stage ^ 1);
+    for (int it = 0;; ++it) {
+        const int t = (int)rank + it * S;
+        if (t >= tiles) break;
+        const int stage = it & 1;
+        if (t + S < tiles) {
+            load_tile(t + S, stage ^ 1);
             cp_wait<1>();
         } else {
             cp_wait<0>();
@@ -276,38 +278,37 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
             o[i][2] *= al_b;
             o[i][3] *= al_b;
         }
-        // O += P V, P split into bf16 hi + lo; keys 16 kk .. 16 kk + 15 per k-step
+        // O += P V with P split into bf16 hi + lo halves (P ~ hi + lo to ~16 bits);
+        // keys 16 kk .. 16 kk + 15 per k-step
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            uint32_t ph[4], pl[4];
-            {
-                const float* s0 = sc[2 * kk];
-                const float* s1 = sc[2 * kk + 1];
-                const float src[8] = {s0[0], s0[1], s0[2], s0[3], s1[0], s1[1], s1[2], s1[3]};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    ph[e] = pack_bf16(src[2 * e], src[2 * e + 1]);
-                    const float2 hv = unpack_bf16(ph[e]);
-                    pl[e] = pack_bf16(src[2 * e] - hv.x, src[2 * e + 1] - hv.y);
-                }
-            }
+            const float* s0 = sc[2 * kk];
+            const float* s1 = sc[2 * kk + 1];
+            const float src[8] = {s0[0], s0[1], s0[2], s0[3], s1[0], s1[1], s1[2], s1[3]};
             // A fragment order: (rows a, keys lo) (rows b, keys lo) (rows a, keys hi) (rows b, keys hi)
-            const uint32_t A0h = ph[0], A1h = ph[1], A2h = ph[2], A3h = ph[3];
-            const uint32_t A0l = pl[0], A1l = pl[1], A2l = pl[2], A3l = pl[3];
+            uint32_t ph[4], pl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                ph[e] = pack_bf16(src[2 * e], src[2 * e + 1]);
+                const float hx = __uint_as_float(ph[e] << 16), hy = __uint_as_float(ph[e] & 0xFFFF0000u);
+                pl[e] = pack_bf16(src[2 * e] - hx, src[2 * e + 1] - hy);
+            }
             const int vrow = 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
             for (int hb = 0; hb < NB_O; hb += 2) {
                 // matrices: (keys 0-7, dims hb), (keys 8-15, dims hb), (keys 0-7, dims hb+1), (keys 8-15, dims hb+1)
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4_t(vbase + swz<HD>(vrow, hb + (lane >> 4)), b0, b1, b2, b3);
-                mma_bf16(o[hb], A0h, A1h, A2h, A3h, b0, b1);
-                mma_bf16(o[hb], A0l, A1l, A2l, A3l, b0, b1);
-                mma_bf16(o[hb + 1], A0h, A1h, A2h, A3h, b2, b3);
-                mma_bf16(o[hb + 1], A0l, A1l, A2l, A3l, b2, b3);
+                mma_bf16(o[hb], ph[0], ph[1], ph[2], ph[3], b0, b1);
+                mma_bf16(o[hb], pl[0], pl[1], pl[2], pl[3], b0, b1);
+                mma_bf16(o[hb + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+                mma_bf16(o[hb + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
             }
         }
         __syncthreads();  // the stage is overwritten by the next prefetch
     }
+    cp_wait<0>();  // an early tile load that was not needed must land before the memory is reused
+    __syncthreads();
 
     // ---- merge the splits and write
     float* Op = reinterpret_cast<float*>(sm);       // [QV][HD]
@@ -328,48 +329,46 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
             Lp[qb] = l_b;
         }
         csync();
+        // rank r merges query vectors [r * vper, (r + 1) * vper): each thread takes one
+        // (vector, 4-dim chunk), loads every rank's (max, sum, O chunk) at once (one DSMEM
+        // round trip) and combines them in rank order
         const int vper = QV / S + ((QV % S) ? 1 : 0);
         const int v0 = (int)rank * vper, v1 = min(QV, v0 + vper);
-        // combination weight of every rank for each query vector this rank owns
-        for (int v = v0 + tid; v < v1; v += NTHR) {
-            float ms[8], ls[8], mstar = -INFINITY;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                ms[q] = q < S ? ld_peer(Mp + v, (uint32_t)q) : -INFINITY;
-                ls[q] = q < S ? ld_peer(Lp + v, (uint32_t)q) : 0.f;
-                mstar = fmaxf(mstar, ms[q]);
-            }
-            float den = 0.f;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (ms[q] != -INFINITY) den += exp2f(ms[q] - mstar) * ls[q];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                wsm[v - v0][q] = (ms[q] != -INFINITY && den > 0.f) ? exp2f(ms[q] - mstar) / den : 0.f;
-        }
-        __syncthreads();
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
         constexpr int C4 = HD / 4;
         for (int idx = tid; idx < (v1 - v0) * C4; idx += NTHR) {
             const int v = v0 + idx / C4, d = 4 * (idx % C4);
-            if (v >= nv) continue;
             const int r = r0 + v / g, h = kvh * g + v % g;
-            if (p.row_seq[r] < 0) continue;
+            const bool live = v < nv && p.row_seq[r] >= 0;
+            float ms[SMAX], ls[SMAX];
+            float4 x[SMAX];
+#pragma unroll
+            for (int q = 0; q < SMAX; ++q) {
+                const bool in = q < S;
+                ms[q] = in ? ld_peer(Mp + v, (uint32_t)q) : -INFINITY;
+                ls[q] = in ? ld_peer(Lp + v, (uint32_t)q) : 0.f;
+                x[q] = in ? ld_peer4(Op + v * HD + d, (uint32_t)q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float mstar = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < SMAX; ++q) mstar = fmaxf(mstar, ms[q]);
+            float den = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float w = wsm[v - v0][q];
-                if (q < S && w != 0.f) {
-                    const float4 x = ld_peer4(Op + v * HD + d, (uint32_t)q);
-                    acc.x += w * x.x;
-                    acc.y += w * x.y;
-                    acc.z += w * x.z;
-                    acc.w += w * x.w;
-                }
+            for (int q = 0; q < SMAX; ++q) {
+                const float e = ms[q] != -INFINITY ? exp2f(ms[q] - mstar) : 0.f;
+                den += e * ls[q];
+                acc.x += e * x[q].x;
+                acc.y += e * x[q].y;
+                acc.z += e * x[q].z;
+                acc.w += e * x[q].w;
             }
-            __nv_bfloat16* dst = out + (size_t)r * p.H * HD + (size_t)h * HD + d;
-            *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x, acc.y);
-            *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z, acc.w);
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            if (live) {
+                __nv_bfloat16* dst = out + (size_t)r * p.H * HD + (size_t)h * HD + d;
+                *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+                *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+            }
         }
         csync();
     } else {
@@ -399,12 +398,15 @@ void run_mma(const Launch& L, const AttnParams& p, int sms) {
     const int cap_tiles = (p.max_keys + KT - 1) / KT;
     const int base = n_groups * p.Hkv;
     int S = 1;
-    while (S < 8 && S * 2 <= cap_tiles && base * S * 2 <= 2 * sms) S *= 2;
+    // (each rank keeps at least two tiles of capacity: below that the wider merge costs
+    // more than the tile it saves)
+    while (S < SMAX && S * 2 <= cap_tiles && base * S * 2 <= 2 * sms) S *= 2;
     a.splits = S;
     using SM = AttnSmem<HD>;
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(attn_mma_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::TOTAL);
+        cudaFuncSetAttribute(attn_mma_kernel<HD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         attr = true;
     }
     launch_k(L, attn_mma_kernel<HD>, dim3(n_groups, p.Hkv, S), dim3(NTHR), (size_t)SM::TOTAL, S, a);

@@ -180,6 +180,8 @@ struct AttnParams {
     int extra;
     int rows;
     int group_rows;       // rows per query group (all from one sequence)
+    int seq_div = 0;      // > 0: rows are sequence-major with seq_div rows each, so the sequence of
+                          // row r is r / seq_div (row_seq < 0 still marks an inactive sequence)
     int H, Hkv, hd;
     int max_keys;         // host upper bound on keys seen by any row
     void* out;            // T [rows, H*hd]
