@@ -835,6 +835,15 @@ bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W,
     else if (M <= 128) MT = 128;
     else MT = 256;
     if (norm_a && MT > 32) return false;  // the fused norm serves blocks of at most 32 rows
+    if (!norm_a) {
+        // Narrower token tiles while the grid is under one wave and the narrower grid still
+        // fits in one (tiles of <= 64 tokens run two CTAs per SM, so one CTA's epilogue
+        // overlaps the other's main loop).
+        const int n_tiles = (N + BN - 1) / BN, sms = sm_count();
+        auto tiles = [&](int mt) { return n_tiles * ((M + mt - 1) / mt); };
+        auto slots = [&](int mt) { return sms * (mt <= 64 ? 2 : 1); };
+        while (MT > 64 && tiles(MT) < slots(MT) && tiles(MT / 2) <= slots(MT / 2)) MT /= 2;
+    }
     CUtensorMap mw, mx;
     if (!make_map(&mw, W, N, K, K, BN)) return false;
     if (norm_a) {

@@ -2,7 +2,8 @@
 inputs.
 
 fp32 workloads: tokens, acceptance lengths and committed lengths bit-exact;
-logits within max-abs 1e-3.  bf16 workloads: logits within max-abs 5e-2,
+logits within max-abs 1e-3.  bf16 workloads: logits within max-abs 5e-2 (scaled by
+weight std / 0.02 for workloads drawn wider than N(0, 0.02)),
 final hidden states within rel-L2 1e-2, tokens identical except where the
 oracle's top-2 logit margin is below 5e-2 (after such a position the two
 streams may diverge, so the comparison stops there).  The oracle never sees
@@ -35,7 +36,7 @@ def _session(w, **kw):
     return Session(w, **kw)
 
 
-def _tokens_match(gpu_tok, ora_logits, bf16):
+def _tokens_match(gpu_tok, ora_logits, bf16, near=BF16_MARGIN):
     """Compare argmax tokens; in bf16 return the first index where a mismatch
     sits at a near-tie (-1 if none).  A mismatch at a clear margin fails."""
     ora_tok = np.argmax(ora_logits, axis=-1)
@@ -45,7 +46,7 @@ def _tokens_match(gpu_tok, ora_logits, bf16):
     margin = spec.top2_margin(ora_logits)
     bad = np.nonzero(gpu_tok != ora_tok)[0]
     for i in bad:
-        assert margin[i] < BF16_MARGIN, f"token {i}: gpu {gpu_tok[i]} oracle {ora_tok[i]} margin {margin[i]}"
+        assert margin[i] < near, f"token {i}: gpu {gpu_tok[i]} oracle {ora_tok[i]} margin {margin[i]}"
     return int(bad[0]) if len(bad) else -1
 
 
@@ -62,7 +63,11 @@ def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), **wkw):
     if wkw:
         w = w.with_(**wkw)
     bf16 = w.dtype == "bf16"
-    ltol = BF16_LOGIT_TOL if bf16 else F32_LOGIT_TOL
+    # bf16 rounding is relative, so the logit tolerance (stated for N(0, 0.02) weights)
+    # scales with the weight std, i.e. with the logit magnitude
+    scale = max(1.0, w.weight_std / 0.02)
+    ltol = BF16_LOGIT_TOL * scale if bf16 else F32_LOGIT_TOL
+    near = BF16_MARGIN * scale
     m = om.Model(w)
     prompts = synth.prompts(w)
     n_ar = 1 + rounds * w.block_size + 1
@@ -76,7 +81,7 @@ def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), **wkw):
         plog = sess.logits("prefill")
         for s, st in enumerate(states):
             assert np.abs(plog[s] - st.first_logits).max() <= ltol
-            if _tokens_match(first[s:s + 1], st.first_logits[None], bf16) >= 0:
+            if _tokens_match(first[s:s + 1], st.first_logits[None], bf16, near) >= 0:
                 alive[s] = False
         # context K/V after prefill
         for s, st in enumerate(states):
@@ -98,7 +103,7 @@ def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), **wkw):
                 od, odl = spec.draft(m, st)
                 if dlog is not None:
                     assert np.abs(dlog[s] - odl).max() <= ltol, f"round {r} seq {s} draft logits"
-                    _tokens_match(drafts[s], odl[1:], bf16)      # mismatches only at near-ties
+                    _tokens_match(drafts[s], odl[1:], bf16, near)      # mismatches only at near-ties
                 proposals.append(props[s](st, od))
             prop = np.stack(proposals).astype(np.int32) if w.block_size > 1 else np.zeros((len(states), 1), np.int32)
             acc, bon = sess.verify(prop)
@@ -111,7 +116,7 @@ def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), **wkw):
                 n0 = st.committed
                 rd = spec.verify(m, st, prop[s][: w.block_size - 1], keep_logits=True)
                 assert np.abs(vlog[s] - rd.verify_logits).max() <= ltol, f"round {r} seq {s} verify logits"
-                _tokens_match(post[s], rd.verify_logits, bf16)
+                _tokens_match(post[s], rd.verify_logits, bf16, near)
                 if acc[s] != rd.accepted or bon[s] != rd.bonus:
                     assert bf16, f"round {r} seq {s}: accepted/bonus differ in fp32"
                     alive[s] = False                             # exempted near-tie changed the stream
