@@ -117,10 +117,11 @@ def measured_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=None) -> str:
+    """Hash of the kernel sources (the listed csrc files, or all of them)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_diffusion_speculative_ctx_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files if files else os.listdir(csrc)):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -133,7 +134,7 @@ def ncu_traffic(kernel_class: str, workload: str):
         return None
     d = json.load(open(p))
     e = d.get(workload, {}).get(kernel_class)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(e.get("sources")):
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -671,18 +671,33 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
             }
         }
         if (a.epi == 1) {
-            // thread e: feature r = e % 64 (gate row r, up row r + 64) of tokens j0 + e / 64, +2, ...
+            // thread e: feature r = e % 64 (gate row r, up row r + 64) of tokens j0 + e / 64, +2, ...;
+            // four tokens per iteration as independent chains (one warp per scheduler here)
             const int e = threadIdx.x - 64;
             const int r = e & 63;
             const int f = 64 * nt + r;
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + f;
+            const size_t ldo = (size_t)a.ldo;
+            const int jend = min(j1, a.M - m0);
+            // silu(g) * u with the fast exponential and division (a gate below about -88 gives
+            // an infinite denominator and a zero result, the function's limit)
+            auto swiglu = [](float gte, float up) { return __fdividef(gte, 1.f + __expf(-gte)) * up; };
             if (n0 + r < a.N) {
-                for (int j = j0 + (e >> 6); j < j1; j += 2) {
-                    const int m = m0 + j;
-                    if (m >= a.M) break;
-                    const float gte = xch[j * BN + r], up = xch[j * BN + r + 64];
-                    out[(size_t)m * a.ldo + f] = __float2bfloat16_rn(gte / (1.f + expf(-gte)) * up);
+                int j = j0 + (e >> 6);
+                for (; j + 6 < jend; j += 8) {
+                    float gv[4], uv[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        gv[t] = xch[(j + 2 * t) * BN + r];
+                        uv[t] = xch[(j + 2 * t) * BN + r + 64];
+                    }
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        out[(size_t)(m0 + j + 2 * t) * ldo] = __float2bfloat16_rn(swiglu(gv[t], uv[t]));
                 }
+                for (; j < jend; j += 2)
+                    out[(size_t)(m0 + j) * ldo] =
+                        __float2bfloat16_rn(swiglu(xch[j * BN + r], xch[j * BN + r + 64]));
             }
         }
     }

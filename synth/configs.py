@@ -125,6 +125,15 @@ def _build() -> dict:
     w["small_bf16_llama_b12"] = w["small_bf16_llama"].with_(
         name="small_bf16_llama_b12", batch=12, prompt_lens=(64, 5, 130, 33, 17, 90, 41, 8, 120, 77, 3, 50),
         weight_std=0.04, prompt_seed=12)
+    # --- profiling shapes: Qwen3-8B layers, head and embedding at reduced depth (3 target
+    # layers, 1 draft layer, features from all three), a few GB on the device, for detailed
+    # profiler captures of the same kernel launches as the full-depth workloads ---
+    _q3 = dict(_QWEN8B, target_layers=3, draft_layers=1, ctx_layer_ids=(0, 1, 2))
+    w["qwen3_8b_shapes_b1_p512_3l"] = Workload(name="qwen3_8b_shapes_b1_p512_3l", batch=1, prompt_lens=(512,),
+                                               max_new_tokens=64, **_q3)
+    w["qwen3_8b_shapes_c32_ragged_3l"] = Workload(name="qwen3_8b_shapes_c32_ragged_3l", batch=32,
+                                                  prompt_lens=_ragged_lengths(1, 32, 256, 2048),
+                                                  max_new_tokens=64, **_q3)
     return w
 
 
