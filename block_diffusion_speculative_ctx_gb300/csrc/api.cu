@@ -78,6 +78,7 @@ struct dflash_ctx {
     int R = 0;  // row capacity
     float* x = nullptr;
     void* xn = nullptr;
+    void* xn_ctx = nullptr;  // normalised operand of the context append (its own: it may run concurrently)
     float* qkv = nullptr;
     void* q = nullptr;
     void* att = nullptr;
@@ -142,6 +143,11 @@ struct dflash_ctx {
     };
     GraphSlot g_draft[2], g_verify;
     cudaStream_t cap_stream = nullptr;
+    // The context append of a draft pass runs on `side_stream`, forked from and joined back
+    // into the pass's stream: draft layer l waits only for ctx_ev[l] (its context K/V).
+    cudaStream_t side_stream = nullptr;
+    std::vector<cudaEvent_t> ctx_ev;  // [Ld] per-layer done, [Ld] fork point
+    bool append_forked = false;
     bool graphs = true;
     std::vector<cudaEvent_t> prof_ev;
     int prof_next = 0;
@@ -376,14 +382,15 @@ struct Pass {
     // RMSNorm kernel writes the bf16/fp32 operand first.
     void normed_gemm(int kind, int rows, const float* x, const float* norm_w, const float* ss_in, const T* W, int N,
                      int K, float* C, int ldc, T* out, int ldo, unsigned long long* keys = nullptr,
-                     const QkvStoreEpi* qkv = nullptr) {
+                     const QkvStoreEpi* qkv = nullptr, void* xbuf = nullptr) {
+        void* xn = xbuf ? xbuf : c->xn;
         Launch L = c->L();
         const double R = rows, es = c->esz;
         const double bytes = (double)N * K * es + R * K * 4 + (out ? R * ldo * es : R * N * 4.0);
         const bool fused = is_bf16 && rows <= 32;
         if (!fused)
             timed(c, DFLASH_K_NORM, R * K * (4 + es), 0, [&] {
-                rmsnorm_rows<T>(L, x, K, norm_w, rows, K, c->cfg.rms_eps, (T*)c->xn, K);
+                rmsnorm_rows<T>(L, x, K, norm_w, rows, K, c->cfg.rms_eps, (T*)xn, K);
             });
         timed(c, kind, bytes, 2 * R * N * (double)K, [&] {
             if constexpr (sizeof(T) == 2) {
@@ -407,9 +414,9 @@ struct Pass {
                     e.keys = keys;
                 }
                 e.qkv = qkv;
-                if (!gemm_tc(L, (const bf16*)c->xn, K, rows, (const bf16*)W, rows, N, K, C, ldc, false, &e)) L.fail();
+                if (!gemm_tc(L, (const bf16*)xn, K, rows, (const bf16*)W, rows, N, K, C, ldc, false, &e)) L.fail();
             } else {
-                gemm<T>(L, (const T*)c->xn, K, W, rows, N, K, C, ldc, false);
+                gemm<T>(L, (const T*)xn, K, W, rows, N, K, C, ldc, false);
             }
         });
     }
@@ -516,6 +523,9 @@ struct Pass {
             ap.out = c->att;
             ap.ws = c->attn_ws;
             ap.ws_bytes = ATTN_WS_BYTES;
+            // the draft's attention reads this layer's context K/V, appended on the side stream
+            if (!target && c->append_forked && cudaStreamWaitEvent(c->stream, c->ctx_ev[l], 0) != cudaSuccess)
+                c->launch_failed = true;
             timed(c, DFLASH_K_ATTENTION, keys_total * 2 * c->kvd * es + 2 * R * c->qd * es,
                   4.0 * R * c->H * c->hd * (keys_total / std::max(1.0, (double)c->batch)), [&] { attention<T>(L, ap); });
             residual_gemm(DFLASH_K_GEMM_O, rows, (const T*)c->att, c->qd, (const T*)w.wo, c->qd);
@@ -539,7 +549,7 @@ struct Pass {
 
     // Context feature rms(W_c stage) and its K/V in every draft layer, stored
     // at (ctx_seq, ctx_pos); rows with ctx_seq < 0 are skipped.
-    void append_context(int rows, const int* ctx_seq, const int* ctx_pos) {
+    void append_context(int rows, const int* ctx_seq, const int* ctx_pos, cudaEvent_t* layer_done = nullptr) {
         Launch L = c->L();
         const double R = rows, d = c->d, es = c->esz;
         timed(c, DFLASH_K_GEMM_FC, gemm_bytes(c, R, d, c->k * d, false), 2 * R * d * c->k * d, [&] {
@@ -563,7 +573,7 @@ struct Pass {
             const QkvStoreEpi qe = qkv_epi(0, nullptr, w.k_norm, elem<T>(c->dK, (size_t)l * c->kv.layer_stride),
                                            elem<T>(c->dV, (size_t)l * c->kv.layer_stride), ctx_seq, ctx_pos);
             normed_gemm(DFLASH_K_GEMM_CTX_KV, rows, c->fcout, c->fc_norm, c->ss_fc, wkv, 2 * c->kvd, c->d, c->kvout,
-                        2 * c->kvd, nullptr, 0, nullptr, fuse_kv ? &qe : nullptr);
+                        2 * c->kvd, nullptr, 0, nullptr, fuse_kv ? &qe : nullptr, c->xn_ctx);
             QKVStore st;
             st.qkv = c->kvout;
             st.ld = 2 * c->kvd;
@@ -589,6 +599,7 @@ struct Pass {
             st.err = c->errw;
             if (!fuse_kv)
                 timed(c, DFLASH_K_ROPE_STORE, R * 2.0 * c->kvd * (4 + es), 0, [&] { qk_norm_rope_store<T>(L, st); });
+            if (layer_done && cudaEventRecord(layer_done[l], c->stream) != cudaSuccess) c->launch_failed = true;
         }
     }
 
@@ -648,11 +659,27 @@ struct Pass {
     void draft() {
         Launch L = c->L();
         const int b = c->batch, B = c->B, g = c->H / c->Hkv;
+        c->append_forked = false;
         if (c->pending_append) {
-            append_context(b * B, c->ctx_row_seq, c->ctx_row_pos);
+            if (is_bf16 && !c->profiling && c->side_stream) {
+                // fork: the append streams its weights while the draft layers run
+                cudaStream_t main = c->stream;
+                if (cudaEventRecord(c->ctx_ev[c->Ld], main) != cudaSuccess ||
+                    cudaStreamWaitEvent(c->side_stream, c->ctx_ev[c->Ld], 0) != cudaSuccess)
+                    c->launch_failed = true;
+                c->stream = c->side_stream;
+                append_context(b * B, c->ctx_row_seq, c->ctx_row_pos, c->ctx_ev.data());
+                c->stream = main;
+                c->append_forked = true;
+            } else {
+                append_context(b * B, c->ctx_row_seq, c->ctx_row_pos);
+            }
             c->pending_append = false;
         }
-        if (B == 1) return;
+        if (B == 1) {
+            join_append();
+            return;
+        }
         timed(c, DFLASH_K_OTHER, (double)b * B * c->d * (4 + c->esz), 0, [&] {
             block_rows(L, b, B, c->n, c->anchor, nullptr, c->cfg.mask_token, c->V, c->max_seq, c->tokens, c->row_seq,
                        c->row_pos, c->errw);
@@ -663,8 +690,16 @@ struct Pass {
         double keys = 0;
         for (int s = 0; s < b; ++s) keys += c->n_upper[s] + B;
         layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, false, keys, B);
+        join_append();  // (already joined by the last layer's attention; kept for clarity)
         // drafts[s][j] = argmax of row s*B + 1 + j
         head(0, b * B, c->draft_norm, c->drafts, c->keep_draft, B);
+    }
+
+    // The pass's stream waits for the whole forked append (its last event).
+    void join_append() {
+        if (!c->append_forked) return;
+        if (cudaStreamWaitEvent(c->stream, c->ctx_ev[c->Ld - 1], 0) != cudaSuccess) c->launch_failed = true;
+        c->append_forked = false;
     }
 
     void verify() {
@@ -937,6 +972,7 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     const size_t R = c->R;
     ALLOC(c->x, R * d * 4);
     ALLOC(c->xn, R * d * esz);
+    ALLOC(c->xn_ctx, R * d * esz);
     ALLOC(c->qkv, R * c->qkv_n * 4);
     ALLOC(c->q, R * c->qd * esz);
     ALLOC(c->att, R * c->qd * esz);
@@ -996,6 +1032,17 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
         c->fail(DFLASH_E_CUDA, "stream creation failed");
         return bail(DFLASH_E_CUDA);
     }
+    if (cudaStreamCreateWithFlags(&c->side_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        c->fail(DFLASH_E_CUDA, "stream creation failed");
+        return bail(DFLASH_E_CUDA);
+    }
+    c->ctx_ev.assign(c->Ld + 1, nullptr);
+    for (auto& e : c->ctx_ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            e = nullptr;
+            c->fail(DFLASH_E_CUDA, "event creation failed");
+            return bail(DFLASH_E_CUDA);
+        }
     c->graphs = (cfg->flags & DFLASH_FLAG_NO_GRAPHS) == 0;
     memset(c->prof_acc, 0, sizeof c->prof_acc);
     if ((cfg->flags & DFLASH_FLAG_PROFILE) && dflash_set_profiling(c, 1) != DFLASH_OK) return bail(DFLASH_E_CUDA);
@@ -1241,6 +1288,9 @@ void dflash_destroy(dflash_ctx* c) {
     reset_graph(c->g_draft[1]);
     reset_graph(c->g_verify);
     if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+    for (auto& e : c->ctx_ev)
+        if (e) cudaEventDestroy(e);
+    if (c->side_stream) cudaStreamDestroy(c->side_stream);
     delete c;
 }
 
