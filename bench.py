@@ -200,6 +200,13 @@ def timed_rounds(sess, props_dev, acc_dev, bon_dev, drafts_dev, first: int, coun
     return per, start.elapsed_time(end)
 
 
+def workload_of(args):
+    """The named workload, with the block size overridden by --block."""
+    from synth import configs
+    w = configs.get(args.workload)
+    return w.with_(block_size=args.block) if args.block else w
+
+
 def run_ncu_target(args, local):
     """Short run for profiler launch lists: prefill, then W + K rounds with the
     drafter's own proposals (no stream discovery, no timing output)."""
@@ -212,7 +219,7 @@ def run_ncu_target(args, local):
 
     torch.cuda.set_device(local)
     dbuild.build()
-    w = configs.get(args.workload)
+    w = workload_of(args)
     B, b = w.block_size, w.batch
     sess = Session(w, max_seq_len=max(w.prompt_lens) + (args.warmup + args.steps + 4) * B)
     sess.prefill(synth.prompts(w))
@@ -240,7 +247,7 @@ def run_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dbuild.build()
-    w = configs.get(args.workload)
+    w = workload_of(args)
     B, b = w.block_size, w.batch
     K, W = args.steps, args.warmup
     rounds = W + K
@@ -449,7 +456,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     from synth import configs
-    w = configs.get(args.workload)
+    w = workload_of(args)
     ctx = max(w.prompt_lens)
     try:
         cores = len(os.sched_getaffinity(0))
@@ -490,6 +497,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--block", type=int, default=0, help="block size B (default: the workload's, 16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ncu-target", action="store_true",

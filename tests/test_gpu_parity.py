@@ -166,6 +166,17 @@ def test_small_bf16_llama_batch12_stepwise():
     assert run_stepwise("small_bf16_llama_b12", rounds=3) >= 18    # of 12 x 3
 
 
+@pytest.mark.parametrize("block", [8, 10])
+def test_small_bf16_block_sizes_8_and_10(block):
+    # the LLaMA setup's B = 10 and the smaller block suggested under load
+    assert run_stepwise("small_bf16", rounds=3, block_size=block) >= 3        # of 2 x 3
+
+
+def test_small_bf16_llama_block10_batch4():
+    # GQA 4 with 10-row blocks: query groups of 40 vectors
+    assert run_stepwise("small_bf16_llama", rounds=3, block_size=10) >= 6     # of 4 x 3
+
+
 def test_block_size_one_is_plain_greedy():
     assert run_stepwise("tiny_f32_b3", rounds=5, block_size=1) == 3 * 5
 
