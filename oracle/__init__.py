@@ -12,6 +12,9 @@ spec     prefill / draft / verify / accept loop, plain AR greedy decode,
          planted proposals that fix the number of accepted drafts.
 metrics  acceptance length, cycle latency, speedup, memory accounting,
          context-layer selection.
+sampling rounds at temperature T > 0: draft laws, proposals drawn by
+         inverse CDF from caller-supplied uniforms, acceptance min(1, p/q),
+         residual resampling, bonus draw.
 
 Pins (checked by ``tests/test_oracle_*.py`` against the pages and the
 mathematics, not against this code):
@@ -27,11 +30,16 @@ mathematics, not against this code):
 * acceptance against its characterisation, exhaustively on tiny inputs;
   planted proposals accept exactly the planted count;
 * printed worked values of the review's eq. 3, eq. 4/5 and eq. 11 and the
-  context-layer lists of the workloads.
+  context-layer lists of the workloads;
+* sampling: the inverse-CDF draw's law by exact quadrature, eq. 6 acceptance
+  frequencies, eq. 7's two forms of the residual mass and the review's worked
+  totals, eq. 8 (the emitted token has the target's law) by seeded Monte
+  Carlo, which also rejects resampling from the target on rejection, and the
+  T -> 0 limit equal to the greedy round.
 
 Parity unpinned: the drafter's numerical output as a whole.  No trained draft
 weights exist here, so nothing outside this code fixes what a random-init
 drafter should propose beyond the structural pins above (context injection,
 bidirectional attention, cache reuse and immutability).
 """
-from . import metrics, model, spec  # noqa: F401
+from . import metrics, model, sampling, spec  # noqa: F401
