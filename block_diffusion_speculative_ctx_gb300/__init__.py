@@ -9,6 +9,7 @@ calls raise.
 The functions carry the C names:
 
     dflash_init, dflash_prefill, dflash_draft_block, dflash_verify,
+    dflash_draft_block_sampled, dflash_verify_sampled,
     dflash_generate, dflash_inspect, dflash_destroy, dflash_last_error
 
 ``Session`` wraps them for tests and the benchmark.
@@ -79,7 +80,8 @@ class dflash_profile_entry(ctypes.Structure):
                 ("flops", ctypes.c_double)]
 
 
-EXPORTS = ("dflash_init", "dflash_prefill", "dflash_draft_block", "dflash_verify", "dflash_generate",
+EXPORTS = ("dflash_init", "dflash_prefill", "dflash_draft_block", "dflash_verify", "dflash_draft_block_sampled",
+           "dflash_verify_sampled", "dflash_generate",
            "dflash_inspect", "dflash_set_profiling", "dflash_destroy", "dflash_last_error")
 
 _lib = None
@@ -105,13 +107,16 @@ def load(build_if_missing: bool = False):
     lib.dflash_prefill.argtypes = [P, I32, P, P, P]
     lib.dflash_draft_block.argtypes = [P, P]
     lib.dflash_verify.argtypes = [P, P, P, P]
+    lib.dflash_draft_block_sampled.argtypes = [P, ctypes.c_float, P, P]
+    lib.dflash_verify_sampled.argtypes = [P, ctypes.c_float, P, P, P, P]
     lib.dflash_generate.argtypes = [P, I32, P, P, I32, P, P, ctypes.POINTER(dflash_stats)]
     lib.dflash_inspect.argtypes = [P, I32, I32, I32, P, SZ, ctypes.POINTER(SZ)]
     lib.dflash_set_profiling.argtypes = [P, I32]
     lib.dflash_destroy.argtypes = [P]
     lib.dflash_last_error.argtypes = [P]
     lib.dflash_last_error.restype = ctypes.c_char_p
-    for f in ("dflash_init", "dflash_prefill", "dflash_draft_block", "dflash_verify", "dflash_generate",
+    for f in ("dflash_init", "dflash_prefill", "dflash_draft_block", "dflash_verify", "dflash_draft_block_sampled",
+              "dflash_verify_sampled", "dflash_generate",
               "dflash_inspect", "dflash_set_profiling"):
         getattr(lib, f).restype = ctypes.c_int
     lib.dflash_destroy.restype = None
@@ -163,6 +168,15 @@ def dflash_draft_block(ctx, draft_tokens) -> int:
 
 def dflash_verify(ctx, draft_tokens, accepted, bonus) -> int:
     return load().dflash_verify(ctx, _ptr(draft_tokens), _ptr(accepted), _ptr(bonus))
+
+
+def dflash_draft_block_sampled(ctx, temperature, u_draft, draft_tokens) -> int:
+    return load().dflash_draft_block_sampled(ctx, float(temperature), _ptr(u_draft), _ptr(draft_tokens))
+
+
+def dflash_verify_sampled(ctx, temperature, draft_tokens, u_verify, accepted, emitted) -> int:
+    return load().dflash_verify_sampled(ctx, float(temperature), _ptr(draft_tokens), _ptr(u_verify), _ptr(accepted),
+                                        _ptr(emitted))
 
 
 def dflash_generate(ctx, prompt_lens, prompt_tokens, max_new_tokens, out_tokens, out_lens, stats=None) -> int:

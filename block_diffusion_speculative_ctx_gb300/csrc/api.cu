@@ -13,6 +13,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <string>
 #include <vector>
 
@@ -86,6 +87,15 @@ struct dflash_ctx {
     void* hmid = nullptr;
     void* stage = nullptr;
     float* fcout = nullptr;
+    // temperature sampling: draft logits kept for verify, softmax row statistics,
+    // uniforms and temperatures (device memory, so captured graphs stay valid)
+    float* dlogits = nullptr;
+    float2* dstat = nullptr;
+    float2* tstat = nullptr;
+    float* u_draft = nullptr;
+    float* u_verify = nullptr;
+    float* temp_dev = nullptr;
+    bool draft_sampled = false;
     void* feat = nullptr;
     float* ss_x = nullptr;   // [ss_tiles][R]: per-128-column sums of squares of x rows (fused norms)
     float* ss_fc = nullptr;  // same for fcout
@@ -141,7 +151,7 @@ struct dflash_ctx {
         long long kernels = 0;
         int eager_runs = 0;
     };
-    GraphSlot g_draft[2], g_verify;
+    GraphSlot g_draft[2], g_verify, g_draft_s[2], g_verify_s;
     cudaStream_t cap_stream = nullptr;
     // The context append of a draft pass runs on `side_stream`, forked from and joined back
     // into the pass's stream: draft layer l waits only for ctx_ev[l] (its context K/V).
@@ -605,27 +615,30 @@ struct Pass {
 
     // Final norm + shared head + row argmax over `rows` rows of x starting at row0.
     // `block` > 0: draft rows, token ids of rows s*block+j (j >= 1) go to out[s*(block-1)+j-1].
-    void head(int row0, int rows, const float* norm, int* out, float* keep, int block = 0) {
+    // `logits_to` set: the fp32 logits are written there (the sampled passes), else to
+    // c->logits only when kept (bf16) or always (fp32, whose argmax reads them).
+    void head(int row0, int rows, const float* norm, int* out, float* keep, int block = 0, float* logits_to = nullptr) {
         Launch L = c->L();
         const double R = rows, V = c->V;
+        float* lg = logits_to ? logits_to : c->logits;
         if (is_bf16) {
-            // head GEMM with the argmax in its epilogue (logits written only when kept)
+            // head GEMM with the argmax in its epilogue (logits written only when needed)
             cudaMemsetAsync(c->keys, 0, (size_t)rows * sizeof(unsigned long long), c->stream);
             normed_gemm(DFLASH_K_GEMM_HEAD, rows, c->x + (size_t)row0 * c->d, norm, c->ss_x + row0,
-                        (const T*)c->head, c->V, c->d, keep ? c->logits : nullptr, c->V, nullptr, 0, c->keys);
+                        (const T*)c->head, c->V, c->d, (keep || logits_to) ? lg : nullptr, c->V, nullptr, 0, c->keys);
             timed(c, DFLASH_K_ARGMAX, R * 8, 0, [&] { keys_to_ids(L, c->keys, rows, block, out); });
         } else {
             normed_gemm(DFLASH_K_GEMM_HEAD, rows, c->x + (size_t)row0 * c->d, norm, c->ss_x + row0,
-                        (const T*)c->head, c->V, c->d, c->logits, c->V, nullptr, 0);
+                        (const T*)c->head, c->V, c->d, lg, c->V, nullptr, 0);
             if (block > 0) {
-                timed(c, DFLASH_K_ARGMAX, R * V * 4, 0, [&] { argmax_rows(L, c->logits, c->V, rows, c->V, c->argbuf); });
+                timed(c, DFLASH_K_ARGMAX, R * V * 4, 0, [&] { argmax_rows(L, lg, c->V, rows, c->V, c->argbuf); });
                 cudaMemcpy2DAsync(out, (size_t)(block - 1) * 4, c->argbuf + 1, (size_t)block * 4,
                                   (size_t)(block - 1) * 4, rows / block, cudaMemcpyDeviceToDevice, c->stream);
             } else {
-                timed(c, DFLASH_K_ARGMAX, R * V * 4, 0, [&] { argmax_rows(L, c->logits, c->V, rows, c->V, out); });
+                timed(c, DFLASH_K_ARGMAX, R * V * 4, 0, [&] { argmax_rows(L, lg, c->V, rows, c->V, out); });
             }
         }
-        if (keep) cudaMemcpyAsync(keep, c->logits, (size_t)rows * c->V * 4, cudaMemcpyDeviceToDevice, c->stream);
+        if (keep) cudaMemcpyAsync(keep, lg, (size_t)rows * c->V * 4, cudaMemcpyDeviceToDevice, c->stream);
     }
 
     dflash_status prefill(int batch, const int* lens, const int* toks, int* first) {
@@ -656,7 +669,8 @@ struct Pass {
         return check_device(c);
     }
 
-    void draft() {
+    // Draft pass; `sampled`: proposals drawn from softmax(draft logits / T) (T in device memory).
+    void draft(bool sampled = false) {
         Launch L = c->L();
         const int b = c->batch, B = c->B, g = c->H / c->Hkv;
         c->append_forked = false;
@@ -692,7 +706,11 @@ struct Pass {
         layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, false, keys, B);
         join_append();  // (already joined by the last layer's attention; kept for clarity)
         // drafts[s][j] = argmax of row s*B + 1 + j
-        head(0, b * B, c->draft_norm, c->drafts, c->keep_draft, B);
+        head(0, b * B, c->draft_norm, c->drafts, c->keep_draft, B, sampled ? c->dlogits : nullptr);
+        if (sampled)  // drafts[s][j] = draw from q of row s*B + 1 + j (replaces the argmax)
+            timed(c, DFLASH_K_ARGMAX, (double)b * (B - 1) * c->V * 8, 0, [&] {
+                draft_sample(L, c->dlogits, c->V, b, B, c->temp_dev, c->u_draft, c->dstat, c->drafts);
+            });
     }
 
     // The pass's stream waits for the whole forked append (its last event).
@@ -702,7 +720,8 @@ struct Pass {
         c->append_forked = false;
     }
 
-    void verify() {
+    // Verify pass; `sampled`: acceptance and emission by speculative rejection sampling.
+    void verify(bool sampled = false) {
         Launch L = c->L();
         const int b = c->batch, B = c->B, g = c->H / c->Hkv;
         timed(c, DFLASH_K_OTHER, (double)b * B * c->d * (4 + c->esz), 0, [&] {
@@ -715,11 +734,18 @@ struct Pass {
         layers(true, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, true, keys, B);
         if (c->keep_hidden)
             cudaMemcpyAsync(c->keep_hidden, c->x, (size_t)b * B * c->d * 4, cudaMemcpyDeviceToDevice, c->stream);
-        head(0, b * B, c->final_norm, c->posterior, c->keep_verify);
-        timed(c, DFLASH_K_OTHER, (double)b * B * 8, 0, [&] {
-            accept(L, b, B, c->proposal, c->posterior, c->n, c->anchor, c->accepted, c->bonus, c->ctx_row_seq,
-                   c->ctx_row_pos);
-        });
+        head(0, b * B, c->final_norm, c->posterior, c->keep_verify, 0, sampled ? c->logits : nullptr);
+        if (sampled) {
+            timed(c, DFLASH_K_ARGMAX, (double)b * B * c->V * 8, 0, [&] {
+                verify_sample(L, c->logits, c->dlogits, c->V, b, B, c->temp_dev, c->proposal, c->u_verify, c->tstat,
+                              c->dstat, c->n, c->anchor, c->accepted, c->bonus, c->ctx_row_seq, c->ctx_row_pos);
+            });
+        } else {
+            timed(c, DFLASH_K_OTHER, (double)b * B * 8, 0, [&] {
+                accept(L, b, B, c->proposal, c->posterior, c->n, c->anchor, c->accepted, c->bonus, c->ctx_row_seq,
+                       c->ctx_row_pos);
+            });
+        }
         c->pending_append = true;
     }
 };
@@ -807,20 +833,20 @@ dflash_status run_pass(dflash_ctx* c, dflash_ctx::GraphSlot& g, F&& pass) {
     return DFLASH_OK;
 }
 
-dflash_status do_draft(dflash_ctx* c) {
+dflash_status do_draft(dflash_ctx* c, bool sampled = false) {
     const int with_append = c->pending_append ? 1 : 0;
-    dflash_status s = run_pass(c, c->g_draft[with_append], [&] {
-        if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.draft();
-        else Pass<float>{c}.draft();
+    dflash_status s = run_pass(c, sampled ? c->g_draft_s[with_append] : c->g_draft[with_append], [&] {
+        if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.draft(sampled);
+        else Pass<float>{c}.draft(sampled);
     });
     c->pending_append = false;
     return s;
 }
 
-dflash_status do_verify(dflash_ctx* c) {
-    dflash_status s = run_pass(c, c->g_verify, [&] {
-        if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.verify();
-        else Pass<float>{c}.verify();
+dflash_status do_verify(dflash_ctx* c, bool sampled = false) {
+    dflash_status s = run_pass(c, sampled ? c->g_verify_s : c->g_verify, [&] {
+        if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.verify(sampled);
+        else Pass<float>{c}.verify(sampled);
     });
     if (s != DFLASH_OK) return s;
     c->pending_append = true;
@@ -842,6 +868,25 @@ dflash_status load_proposal(dflash_ctx* c, const int32_t* toks) {
                 return c->fail(DFLASH_E_INVAL, "draft token %zu = %d outside [0, %d)", i, toks[i], c->V);
         CUDA_TRY(c, cudaMemcpyAsync(c->proposal, toks, n * 4, cudaMemcpyHostToDevice, c->stream));
     }
+    return DFLASH_OK;
+}
+
+// Stage n caller uniforms (host or device) into dst; host values must lie in [0, 1).
+dflash_status load_uniforms(dflash_ctx* c, float* dst, const float* u, size_t n) {
+    if (n == 0) return DFLASH_OK;
+    if (is_device_ptr(u)) {
+        CUDA_TRY(c, cudaMemcpyAsync(dst, u, n * 4, cudaMemcpyDeviceToDevice, c->stream));
+    } else {
+        for (size_t i = 0; i < n; ++i)
+            if (!(u[i] >= 0.f && u[i] < 1.f)) return c->fail(DFLASH_E_INVAL, "uniform %zu = %g outside [0, 1)", i, u[i]);
+        CUDA_TRY(c, cudaMemcpyAsync(dst, u, n * 4, cudaMemcpyHostToDevice, c->stream));
+    }
+    return DFLASH_OK;
+}
+
+dflash_status set_temperature(dflash_ctx* c, int which, float t) {
+    if (!(t > 0.f) || !std::isfinite(t)) return c->fail(DFLASH_E_INVAL, "temperature %g is not a positive finite number", t);
+    CUDA_TRY(c, cudaMemcpyAsync(c->temp_dev + which, &t, 4, cudaMemcpyHostToDevice, c->stream));
     return DFLASH_OK;
 }
 
@@ -986,6 +1031,12 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     ALLOC(c->feat, R * d * esz);
     ALLOC(c->kvout, R * 2 * c->kvd * 4);
     ALLOC(c->logits, (size_t)rb * V * 4);
+    ALLOC(c->dlogits, (size_t)rb * V * 4);
+    ALLOC(c->dstat, (size_t)rb * sizeof(float2));
+    ALLOC(c->tstat, (size_t)rb * sizeof(float2));
+    ALLOC(c->u_draft, (size_t)rb * 4);
+    ALLOC(c->u_verify, (size_t)rb * 4);
+    ALLOC(c->temp_dev, 16);
     ALLOC(c->tokens, R * 4);
     ALLOC(c->row_seq, R * 4);
     ALLOC(c->row_pos, R * 4);
@@ -1095,6 +1146,7 @@ dflash_status dflash_draft_block(dflash_ctx* c, int32_t* draft_tokens) {
     dflash_status s;
     if ((s = capacity_check(c))) return s;
     if ((s = do_draft(c))) return s;
+    c->draft_sampled = false;
     bool host = false;
     if (c->B > 1 && draft_tokens != c->drafts)
         if ((s = store_out(c, draft_tokens, c->drafts, (size_t)c->batch * (c->B - 1) * 4, &host))) return s;
@@ -1114,6 +1166,49 @@ dflash_status dflash_verify(dflash_ctx* c, const int32_t* draft_tokens, int32_t*
     bool h1 = false, h2 = false;
     if ((s = store_out(c, accepted, c->accepted, (size_t)c->batch * 4, &h1))) return s;
     if ((s = store_out(c, bonus, c->bonus, (size_t)c->batch * 4, &h2))) return s;
+    if (h1) {
+        if ((s = check_device(c))) return s;
+        for (int i = 0; i < c->batch; ++i) c->n_upper[i] += accepted[i] + 1 - c->B;  // now exact
+    } else if (h2) {
+        if ((s = check_device(c))) return s;
+    }
+    return DFLASH_OK;
+}
+
+dflash_status dflash_draft_block_sampled(dflash_ctx* c, float temperature, const float* u_draft,
+                                        int32_t* draft_tokens) {
+    if (!c) return DFLASH_E_INVAL;
+    if (c->state != ST_READY) return c->fail(DFLASH_E_STATE, c->state == ST_EMPTY ? "draft_block_sampled before prefill" : "draft_block_sampled called twice without verify");
+    if (c->B > 1 && (!draft_tokens || !u_draft)) return c->fail(DFLASH_E_INVAL, "NULL argument");
+    dflash_status s;
+    if ((s = set_temperature(c, 0, temperature))) return s;
+    if ((s = load_uniforms(c, c->u_draft, u_draft, (size_t)c->batch * (c->B - 1)))) return s;
+    if ((s = capacity_check(c))) return s;
+    if ((s = do_draft(c, true))) return s;
+    c->draft_sampled = true;
+    bool host = false;
+    if (c->B > 1 && draft_tokens != c->drafts)
+        if ((s = store_out(c, draft_tokens, c->drafts, (size_t)c->batch * (c->B - 1) * 4, &host))) return s;
+    c->state = ST_DRAFTED;
+    if (host) return check_device(c);
+    return DFLASH_OK;
+}
+
+dflash_status dflash_verify_sampled(dflash_ctx* c, float temperature, const int32_t* draft_tokens,
+                                    const float* u_verify, int32_t* accepted, int32_t* emitted) {
+    if (!c) return DFLASH_E_INVAL;
+    if (c->state != ST_DRAFTED || (!c->draft_sampled && c->B > 1))
+        return c->fail(DFLASH_E_STATE, "verify_sampled needs a preceding draft_block_sampled");
+    if ((!draft_tokens && c->B > 1) || !u_verify || !accepted || !emitted) return c->fail(DFLASH_E_INVAL, "NULL argument");
+    dflash_status s;
+    if ((s = set_temperature(c, 1, temperature))) return s;
+    if ((s = load_uniforms(c, c->u_verify, u_verify, (size_t)c->batch * c->B))) return s;
+    if ((s = load_proposal(c, draft_tokens))) return s;
+    if ((s = do_verify(c, true))) return s;
+    c->state = ST_READY;
+    bool h1 = false, h2 = false;
+    if ((s = store_out(c, accepted, c->accepted, (size_t)c->batch * 4, &h1))) return s;
+    if ((s = store_out(c, emitted, c->bonus, (size_t)c->batch * 4, &h2))) return s;
     if (h1) {
         if ((s = check_device(c))) return s;
         for (int i = 0; i < c->batch; ++i) c->n_upper[i] += accepted[i] + 1 - c->B;  // now exact
@@ -1287,6 +1382,9 @@ void dflash_destroy(dflash_ctx* c) {
     reset_graph(c->g_draft[0]);
     reset_graph(c->g_draft[1]);
     reset_graph(c->g_verify);
+    reset_graph(c->g_draft_s[0]);
+    reset_graph(c->g_draft_s[1]);
+    reset_graph(c->g_verify_s);
     if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
     for (auto& e : c->ctx_ev)
         if (e) cudaEventDestroy(e);

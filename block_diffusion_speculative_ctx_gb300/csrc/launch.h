@@ -193,6 +193,19 @@ void attention(const Launch& L, const AttnParams& p);
 // bf16 path of attention(): tensor cores (mma.sync), cluster-merged key splits.
 void attention_mma(const Launch& L, const AttnParams& p, int sms);
 
+// ---- temperature sampling (sampling.cu)
+// Draft rows s*B + j (j = 1..B-1) of dlogits [batch*B, V]: dstat[row] = (max, sum exp((l - max)/T)),
+// drafts[s*(B-1) + j-1] = inverse-CDF draw of softmax(l/T) with u_draft[s*(B-1) + j-1];
+// temp[0] = draft T (device memory).
+void draft_sample(const Launch& L, const float* dlogits, int V, int batch, int B, const float* temp,
+                  const float* u_draft, float2* dstat, int* drafts);
+// Target-row statistics (temp[1] = verify T), then per sequence: acceptance of the proposals
+// with min(1, p/q) against u_verify[s*B + j], the residual or bonus draw with u_verify[s*B + B-1],
+// and the round's bookkeeping (as accept()).
+void verify_sample(const Launch& L, const float* logits, const float* dlogits, int V, int batch, int B,
+                   const float* temp, const int* proposal, const float* u_verify, float2* tstat, const float2* dstat,
+                   int* n, int* anchor, int* accepted, int* bonus, int* ctx_row_seq, int* ctx_row_pos);
+
 // ---- round bookkeeping
 // Block rows of a draft (proposal == nullptr) or verify pass: token of row
 // s*B+j is anchor[s] (j == 0), the mask id (draft) or proposal[s*(B-1)+j-1]

@@ -1,0 +1,248 @@
+// Temperature sampling of the draft-and-verify round (T > 0): speculative
+// rejection sampling, "DFlash: Why a Diffusion Drafter Can Accelerate an
+// Autoregressive Model" §4.2 (eq. 6-8) and Algorithm 1 (steps 2-3, 7-8, 10);
+// "DFlash: Block Diffusion for Flash Speculative Decoding", Paper vs code
+// "Sampling rule".
+//
+// Laws are softmax(logits / T) of fp32 logit rows: q from the draft head's
+// rows 1..B-1, p from the verify head's rows 0..B-1 (p_j judges the proposal
+// at block row j + 1).  Every draw is an inverse-CDF lookup of a caller-supplied
+// uniform u in [0, 1): the lowest token z whose cumulative weight exceeds
+// u * total.  One CTA handles one row (draws) or one sequence (acceptance and
+// the emitted token); thread t owns the contiguous token chunk
+// [t C, (t + 1) C), so every sum is taken in one fixed order.
+#include <math.h>
+
+#include "launch.h"
+
+namespace dfl {
+
+namespace {
+
+constexpr int SNT = 1024;  // threads per sampling CTA
+
+// Row statistics of softmax(l / T): m = max l, s = sum exp((l - m) / T).
+__device__ float block_max_f(float v, float* red) {
+    v = warp_max(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        v = l < (int)(blockDim.x >> 5) ? red[l] : -INFINITY;
+        v = warp_max(v);
+        if (l == 0) red[0] = v;
+    }
+    __syncthreads();
+    v = red[0];
+    __syncthreads();
+    return v;
+}
+
+__device__ float block_sum_f(float v, float* red) {
+    v = warp_sum(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        v = l < (int)(blockDim.x >> 5) ? red[l] : 0.f;
+        v = warp_sum(v);
+        if (l == 0) red[0] = v;
+    }
+    __syncthreads();
+    v = red[0];
+    __syncthreads();
+    return v;
+}
+
+__device__ void row_stats(const float* __restrict__ row, int V, float inv_t, float* red, float& m, float& s) {
+    const int C = (V + blockDim.x - 1) / blockDim.x;
+    const int z0 = threadIdx.x * C, z1 = min(V, z0 + C);
+    float mx = -INFINITY;
+    for (int z = z0; z < z1; ++z) mx = fmaxf(mx, row[z]);
+    m = block_max_f(mx, red);
+    float acc = 0.f;
+    for (int z = z0; z < z1; ++z) acc += expf((row[z] - m) * inv_t);
+    s = block_sum_f(acc, red);
+}
+
+// Inverse-CDF draw over weights w(z) >= 0 (a functor), u in [0, 1).  Chunk sums,
+// a block-wide exclusive scan of them in thread order, then the thread whose
+// range holds u * total scans its chunk.  Returns -1 when the total weight is 0.
+template <class W>
+__device__ int draw_inverse_cdf(const W& w, int V, float u, float* scan, int* pick) {
+    const int C = (V + blockDim.x - 1) / blockDim.x;
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5, nw = blockDim.x >> 5;
+    const int z0 = t * C, z1 = min(V, z0 + C);
+    float cs = 0.f;
+    for (int z = z0; z < z1; ++z) cs += w(z);
+    // inclusive scan within the warp, then over the warp totals
+    float inc = cs;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += n;
+    }
+    if (lane == 31) scan[wid] = inc;
+    if (t == 0) *pick = -1;
+    __syncthreads();
+    if (wid == 0) {
+        float wt = lane < nw ? scan[lane] : 0.f;
+        float wi = wt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += n;
+        }
+        if (lane < nw) scan[32 + lane] = wi - wt;  // exclusive prefix of warp totals
+        if (lane == nw - 1) scan[64] = wi;         // total
+    }
+    __syncthreads();
+    const float total = scan[64];
+    const float excl = scan[32 + wid] + (inc - cs);
+    const float target = u * total;
+    if (total > 0.f && cs > 0.f && excl <= target && target < excl + cs) {
+        float acc = excl;
+        int zz = -1, last = -1;
+        for (int z = z0; z < z1; ++z) {
+            const float wz = w(z);
+            if (wz > 0.f) last = z;
+            acc += wz;
+            if (acc > target) {
+                zz = z;
+                break;
+            }
+        }
+        atomicMax(pick, zz >= 0 ? zz : last);
+    }
+    __syncthreads();
+    int r = *pick;
+    if (r < 0 && total > 0.f) {
+        // rounding left u * total past every boundary: the last token with weight
+        int lastp = -1;
+        for (int z = z1 - 1; z >= z0; --z)
+            if (w(z) > 0.f) {
+                lastp = z;
+                break;
+            }
+        atomicMax(pick, lastp);
+        __syncthreads();
+        r = *pick;
+    }
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ float clamp_u(float u) { return fminf(fmaxf(u, 0.f), 0.99999994f); }
+
+// Draft rows s*B + j, j = 1..B-1: statistics of q_j and the proposal drawn from it.
+__global__ void __launch_bounds__(SNT) draft_sample_kernel(const float* __restrict__ dlogits, int V, int B,
+                                                           const float* __restrict__ temp,
+                                                           const float* __restrict__ u_draft,
+                                                           float2* __restrict__ dstat, int* __restrict__ drafts) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float red[72];
+    __shared__ int pick;
+    const int k = blockIdx.x, s = k / (B - 1), j = k % (B - 1) + 1;
+    const int row = s * B + j;
+    const float* l = dlogits + (size_t)row * V;
+    const float inv_t = 1.f / temp[0];
+    float m, sum;
+    row_stats(l, V, inv_t, red, m, sum);
+    if (threadIdx.x == 0) dstat[row] = make_float2(m, sum);
+    const int z = draw_inverse_cdf([&](int zz) { return expf((l[zz] - m) * inv_t); }, V, clamp_u(u_draft[k]), red,
+                                   &pick);
+    if (threadIdx.x == 0) drafts[k] = z;
+}
+
+// Target rows: statistics of p_j.
+__global__ void __launch_bounds__(SNT) target_stats_kernel(const float* __restrict__ logits, int V,
+                                                           const float* __restrict__ temp,
+                                                           float2* __restrict__ tstat) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float red[32];
+    const int row = blockIdx.x;
+    float m, sum;
+    row_stats(logits + (size_t)row * V, V, 1.f / temp[1], red, m, sum);
+    if (threadIdx.x == 0) tstat[row] = make_float2(m, sum);
+}
+
+// One sequence: scan the proposals with eq. 6, emit a residual draw (eq. 7) at the
+// first rejection or the bonus draw from p_{B-1}, then the round's bookkeeping
+// (accepted count, emitted token = next anchor, length, context rows to append).
+__global__ void __launch_bounds__(SNT) verify_sample_kernel(
+    const float* __restrict__ logits, const float* __restrict__ dlogits, int V, int B, const float* __restrict__ temp,
+    const int* __restrict__ proposal, const float* __restrict__ u_verify, const float2* __restrict__ tstat,
+    const float2* __restrict__ dstat, int* __restrict__ n, int* __restrict__ anchor, int* __restrict__ accepted,
+    int* __restrict__ bonus, int* __restrict__ ctx_row_seq, int* __restrict__ ctx_row_pos, uint32_t* err) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float scan[72];
+    __shared__ int pick, a_s;
+    const int s = blockIdx.x;
+    const float inv_td = 1.f / temp[0], inv_tv = 1.f / temp[1];
+    const int* prop = proposal + (size_t)s * (B - 1);
+    const float* u = u_verify + (size_t)s * B;
+    if (threadIdx.x == 0) {
+        int a = 0;
+        for (; a < B - 1; ++a) {
+            const int y = prop[a];
+            if (y < 0 || y >= V) {
+                atomicOr(err, ERR_TOKEN_RANGE);
+                break;
+            }
+            const float2 ts = tstat[s * B + a], ds = dstat[s * B + a + 1];
+            const float p = expf((logits[(size_t)(s * B + a) * V + y] - ts.x) * inv_tv) / ts.y;
+            const float q = expf((dlogits[(size_t)(s * B + a + 1) * V + y] - ds.x) * inv_td) / ds.y;
+            const float ratio = q > 0.f ? fminf(1.f, p / q) : 1.f;
+            if (!(clamp_u(u[a]) < ratio)) break;
+        }
+        a_s = a;
+    }
+    __syncthreads();
+    const int a = a_s;
+    const float ue = clamp_u(u[B - 1]);
+    const float* lp = logits + (size_t)(s * B + a) * V;
+    const float2 ts = tstat[s * B + a];
+    auto p_of = [&](int z) { return expf((lp[z] - ts.x) * inv_tv) / ts.y; };
+    int emit = -1;
+    if (a < B - 1) {
+        const float* lq = dlogits + (size_t)(s * B + a + 1) * V;
+        const float2 ds = dstat[s * B + a + 1];
+        emit = draw_inverse_cdf(
+            [&](int z) { return fmaxf(p_of(z) - expf((lq[z] - ds.x) * inv_td) / ds.y, 0.f); }, V, ue, scan, &pick);
+    }
+    if (emit < 0) emit = draw_inverse_cdf(p_of, V, ue, scan, &pick);  // bonus, or a residual of zero mass
+    if (threadIdx.x == 0) {
+        const int n0 = n[s];
+        accepted[s] = a;
+        bonus[s] = emit;
+        anchor[s] = emit;
+        n[s] = n0 + a + 1;
+        for (int j = 0; j < B; ++j) {
+            ctx_row_seq[s * B + j] = (j <= a) ? s : -1;
+            ctx_row_pos[s * B + j] = n0 + j;
+        }
+    }
+}
+
+}  // namespace
+
+void draft_sample(const Launch& L, const float* dlogits, int V, int batch, int B, const float* temp,
+                  const float* u_draft, float2* dstat, int* drafts) {
+    if (batch <= 0 || B < 2) return;
+    launch_k(L, draft_sample_kernel, dim3(batch * (B - 1)), dim3(SNT), 0, 1, dlogits, V, B, temp, u_draft, dstat,
+             drafts);
+}
+
+void verify_sample(const Launch& L, const float* logits, const float* dlogits, int V, int batch, int B,
+                   const float* temp, const int* proposal, const float* u_verify, float2* tstat, const float2* dstat,
+                   int* n, int* anchor, int* accepted, int* bonus, int* ctx_row_seq, int* ctx_row_pos) {
+    if (batch <= 0) return;
+    launch_k(L, target_stats_kernel, dim3(batch * B), dim3(SNT), 0, 1, logits, V, temp, tstat);
+    launch_k(L, verify_sample_kernel, dim3(batch), dim3(SNT), 0, 1, logits, dlogits, V, B, temp, proposal, u_verify,
+             (const float2*)tstat, dstat, n, anchor, accepted, bonus, ctx_row_seq, ctx_row_pos, L.err);
+}
+
+}  // namespace dfl

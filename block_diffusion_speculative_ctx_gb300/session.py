@@ -152,6 +152,30 @@ class Session:
         _check(self.ctx, self.lib.dflash_verify(self.ctx, _ptr(proposal), _ptr(accepted), _ptr(bonus)))
         return accepted, bonus
 
+    def draft_block_sampled(self, temperature: float, u_draft, out=None):
+        """Proposals [batch, B-1] drawn at temperature T with uniforms u_draft [batch, B-1]."""
+        if isinstance(u_draft, np.ndarray):
+            u_draft = np.ascontiguousarray(u_draft, dtype=np.float32)
+        if out is None:
+            out = np.zeros((self.batch, max(self.B - 1, 1)), dtype=np.int32)
+        _check(self.ctx, self.lib.dflash_draft_block_sampled(self.ctx, float(temperature), _ptr(u_draft), _ptr(out)))
+        return out
+
+    def verify_sampled(self, temperature: float, proposal, u_verify, accepted=None, emitted=None):
+        """Speculative rejection sampling of a proposal; u_verify [batch, B] (B-1 acceptance
+        uniforms, then the emission uniform).  Returns (accepted, emitted)."""
+        if isinstance(proposal, np.ndarray):
+            proposal = np.ascontiguousarray(proposal, dtype=np.int32)
+        if isinstance(u_verify, np.ndarray):
+            u_verify = np.ascontiguousarray(u_verify, dtype=np.float32)
+        if accepted is None:
+            accepted = np.zeros(self.batch, dtype=np.int32)
+        if emitted is None:
+            emitted = np.zeros(self.batch, dtype=np.int32)
+        _check(self.ctx, self.lib.dflash_verify_sampled(self.ctx, float(temperature), _ptr(proposal), _ptr(u_verify),
+                                                        _ptr(accepted), _ptr(emitted)))
+        return accepted, emitted
+
     def generate(self, prompts: Sequence[np.ndarray], max_new_tokens: int):
         lens = np.array([len(p) for p in prompts], dtype=np.int32)
         toks = np.ascontiguousarray(np.concatenate([np.asarray(p, dtype=np.int32) for p in prompts]))

@@ -207,6 +207,36 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t* draft_tokens);
 dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* draft_tokens, int32_t* accepted,
                             int32_t* bonus);
 
+/* Temperature sampling (T > 0): speculative rejection sampling ([review] §4.2
+ * eq. 6-8 and Algorithm 1 steps 2-3, 7-8 and 10; [digest] Paper vs code
+ * "Sampling rule").  The method's random numbers are inputs: every draw is
+ * the lowest token z whose cumulative weight exceeds u * total weight, for a
+ * caller-supplied uniform u in [0, 1).  Top-p / top-k are not applied.
+ *
+ * dflash_draft_block_sampled: as dflash_draft_block, then the proposal of
+ * mask row j is drawn from q_j = softmax(draft logits_j / T) with
+ * u_draft[s*(B-1) + j-1]; the laws q are kept for the next verify.
+ * u_draft: [batch, B-1] float, host (each in [0, 1), else E_INVAL) or device
+ * (clamped to [0, 1)); draft_tokens: [batch, B-1] int32 output, host or device.
+ * Errors: as dflash_draft_block, plus E_INVAL (T not positive and finite).
+ *
+ * dflash_verify_sampled: one causal target pass as dflash_verify; with
+ * p_j = softmax(verify logits_j / T), proposal j (block row j+1) is accepted
+ * while u_verify[s*B + j] < min(1, p_j(y)/q_{j+1}(y)); at the first rejection
+ * the emitted token is drawn from [p_a - q_{a+1}]_+ (normalised), else from
+ * p_{B-1}, with u_verify[s*B + B-1].  Caches keep the anchor and the a_i
+ * accepted rows (n_i += a_i + 1); the emitted token is the next anchor.
+ * u_verify: [batch, B] float (host or device, as above); draft_tokens:
+ * [batch, B-1] int32 input (the laws are those of the preceding sampled draft);
+ * accepted, emitted: [batch] int32 outputs, host or device.
+ * Errors: E_STATE (no dflash_draft_block_sampled since the last verify),
+ * E_INVAL (T, NULL, host token or uniform out of range), E_DEVICE_CHECK
+ * (device token outside [0, V): treated as a rejection), E_CUDA. */
+dflash_status dflash_draft_block_sampled(dflash_ctx* ctx, float temperature, const float* u_draft,
+                                        int32_t* draft_tokens);
+dflash_status dflash_verify_sampled(dflash_ctx* ctx, float temperature, const int32_t* draft_tokens,
+                                    const float* u_verify, int32_t* accepted, int32_t* emitted);
+
 /* Greedy speculative generation ([digest] greedy decoding-round pseudocode):
  * prefill, then rounds of draft_block + verify until every sequence has
  * max_new_tokens tokens (the first token counts); each sequence's output is
