@@ -95,6 +95,8 @@ struct dflash_ctx {
     float* u_draft = nullptr;
     float* u_verify = nullptr;
     float* temp_dev = nullptr;
+    float* temp_pinned = nullptr;          // host staging of the two temperatures
+    float temp_cur[2] = {-1.f, -1.f};      // values last written to temp_dev
     bool draft_sampled = false;
     void* feat = nullptr;
     float* ss_x = nullptr;   // [ss_tiles][R]: per-128-column sums of squares of x rows (fused norms)
@@ -884,9 +886,16 @@ dflash_status load_uniforms(dflash_ctx* c, float* dst, const float* u, size_t n)
     return DFLASH_OK;
 }
 
+// The temperature reaches the kernels through device memory (captured passes stay valid);
+// it is copied only when it changes, from pinned memory, after the stream has drained any
+// copy of the previous value.
 dflash_status set_temperature(dflash_ctx* c, int which, float t) {
     if (!(t > 0.f) || !std::isfinite(t)) return c->fail(DFLASH_E_INVAL, "temperature %g is not a positive finite number", t);
-    CUDA_TRY(c, cudaMemcpyAsync(c->temp_dev + which, &t, 4, cudaMemcpyHostToDevice, c->stream));
+    if (c->temp_cur[which] == t) return DFLASH_OK;
+    CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+    c->temp_pinned[which] = t;
+    CUDA_TRY(c, cudaMemcpyAsync(c->temp_dev + which, c->temp_pinned + which, 4, cudaMemcpyHostToDevice, c->stream));
+    c->temp_cur[which] = t;
     return DFLASH_OK;
 }
 
@@ -1037,6 +1046,11 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     ALLOC(c->u_draft, (size_t)rb * 4);
     ALLOC(c->u_verify, (size_t)rb * 4);
     ALLOC(c->temp_dev, 16);
+    if (cudaMallocHost(&c->temp_pinned, 2 * sizeof(float)) != cudaSuccess) {
+        c->temp_pinned = nullptr;
+        c->fail(DFLASH_E_NOMEM, "pinned host allocation failed");
+        return bail(DFLASH_E_NOMEM);
+    }
     ALLOC(c->tokens, R * 4);
     ALLOC(c->row_seq, R * 4);
     ALLOC(c->row_pos, R * 4);
@@ -1389,6 +1403,7 @@ void dflash_destroy(dflash_ctx* c) {
     for (auto& e : c->ctx_ev)
         if (e) cudaEventDestroy(e);
     if (c->side_stream) cudaStreamDestroy(c->side_stream);
+    if (c->temp_pinned) cudaFreeHost(c->temp_pinned);
     delete c;
 }
 

@@ -9,8 +9,8 @@
 // at block row j + 1).  Every draw is an inverse-CDF lookup of a caller-supplied
 // uniform u in [0, 1): the lowest token z whose cumulative weight exceeds
 // u * total.  One CTA handles one row (draws) or one sequence (acceptance and
-// the emitted token); thread t owns the contiguous token chunk
-// [t C, (t + 1) C), so every sum is taken in one fixed order.
+// the emitted token); every pass over a row is coalesced and every sum is taken
+// in one fixed order.
 #include <math.h>
 
 #include "launch.h"
@@ -54,76 +54,110 @@ __device__ float block_sum_f(float v, float* red) {
     return v;
 }
 
-__device__ void row_stats(const float* __restrict__ row, int V, float inv_t, float* red, float& m, float& s) {
-    const int C = (V + blockDim.x - 1) / blockDim.x;
-    const int z0 = threadIdx.x * C, z1 = min(V, z0 + C);
-    float mx = -INFINITY;
-    for (int z = z0; z < z1; ++z) mx = fmaxf(mx, row[z]);
-    m = block_max_f(mx, red);
-    float acc = 0.f;
-    for (int z = z0; z < z1; ++z) acc += expf((row[z] - m) * inv_t);
-    s = block_sum_f(acc, red);
+// Sum of w(z) over z = first, first + stride, ... < end with eight independent
+// partial sums (eight loads in flight per thread), combined in a fixed order.
+template <class W>
+__device__ __forceinline__ float strided_sum(const W& w, int first, int end, int stride) {
+    float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int z = first;
+    for (; z + 7 * stride < end; z += 8 * stride) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) p[k] += w(z + k * stride);
+    }
+    for (int k = 0; z < end; z += stride, ++k) p[k & 7] += w(z);
+    return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
 
-// Inverse-CDF draw over weights w(z) >= 0 (a functor), u in [0, 1).  Chunk sums,
-// a block-wide exclusive scan of them in thread order, then the thread whose
-// range holds u * total scans its chunk.  Returns -1 when the total weight is 0.
+__device__ void row_stats(const float* __restrict__ row, int V, float inv_t, float* red, float& m, float& s) {
+    // coalesced: thread t reads tokens t, t + blockDim, ... (a fixed order for the sum)
+    float mx[8] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    const int st = blockDim.x;
+    int z = threadIdx.x;
+    for (; z + 7 * st < V; z += 8 * st) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], row[z + k * st]);
+    }
+    for (int k = 0; z < V; z += st, ++k) mx[k & 7] = fmaxf(mx[k & 7], row[z]);
+    m = block_max_f(fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))),
+                    red);
+    const float mm = m;
+    s = block_sum_f(strided_sum([&](int zz) { return expf((row[zz] - mm) * inv_t); }, threadIdx.x, V, st), red);
+}
+
+// Inverse-CDF draw over weights w(z) >= 0 (a functor), u in [0, 1): the lowest z whose
+// cumulative weight exceeds u * total.  Warp k owns the contiguous token range
+// [k R, (k + 1) R) and sums it coalesced; the warp sums are scanned in warp order; in
+// the warp whose range holds u * total, lane l sums the contiguous sub-range
+// [l R', (l + 1) R') of it, the lane sums are scanned in lane order, and the lane
+// whose sub-range holds u * total walks it in token order.  Returns -1 when the
+// total weight is 0.
 template <class W>
 __device__ int draw_inverse_cdf(const W& w, int V, float u, float* scan, int* pick) {
-    const int C = (V + blockDim.x - 1) / blockDim.x;
-    const int t = threadIdx.x, lane = t & 31, wid = t >> 5, nw = blockDim.x >> 5;
-    const int z0 = t * C, z1 = min(V, z0 + C);
-    float cs = 0.f;
-    for (int z = z0; z < z1; ++z) cs += w(z);
-    // inclusive scan within the warp, then over the warp totals
-    float inc = cs;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float n = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += n;
-    }
-    if (lane == 31) scan[wid] = inc;
-    if (t == 0) *pick = -1;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int R = ((V + nw - 1) / nw + 31) / 32 * 32;
+    const int z0 = wid * R, z1 = min(V, z0 + R);
+    const float ws = warp_sum(strided_sum(w, z0 + lane, z1, 32));
+    if (lane == 0) scan[wid] = ws;
+    if (threadIdx.x == 0) *pick = -1;
     __syncthreads();
     if (wid == 0) {
-        float wt = lane < nw ? scan[lane] : 0.f;
+        const float wt = lane < nw ? scan[lane] : 0.f;
         float wi = wt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float n = __shfl_up_sync(0xffffffffu, wi, o);
             if (lane >= o) wi += n;
         }
-        if (lane < nw) scan[32 + lane] = wi - wt;  // exclusive prefix of warp totals
+        if (lane < nw) scan[32 + lane] = wi - wt;  // exclusive prefix of the warp sums
         if (lane == nw - 1) scan[64] = wi;         // total
     }
     __syncthreads();
-    const float total = scan[64];
-    const float excl = scan[32 + wid] + (inc - cs);
+    const float total = scan[64], excl = scan[32 + wid];
     const float target = u * total;
-    if (total > 0.f && cs > 0.f && excl <= target && target < excl + cs) {
-        float acc = excl;
-        int zz = -1, last = -1;
-        for (int z = z0; z < z1; ++z) {
-            const float wz = w(z);
-            if (wz > 0.f) last = z;
-            acc += wz;
-            if (acc > target) {
-                zz = z;
-                break;
-            }
+    if (total > 0.f && ws > 0.f && excl <= target && target < excl + ws) {
+        const int R2 = (z1 - z0 + 31) / 32;
+        const int c0 = min(z1, z0 + lane * R2), c1 = min(z1, c0 + R2);
+        const float cs = strided_sum(w, c0, c1, 1);
+        float inc = cs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += n;
         }
-        atomicMax(pick, zz >= 0 ? zz : last);
+        const float ex = excl + (inc - cs);
+        const unsigned hit = __ballot_sync(0xffffffffu, cs > 0.f && ex <= target && target < ex + cs);
+        int found = -1;
+        if (hit && lane == __ffs(hit) - 1) {
+            float acc = ex;
+            int last = -1;
+            for (int z = c0; z < c1; ++z) {
+                const float wz = w(z);
+                if (wz > 0.f) last = z;
+                acc += wz;
+                if (acc > target) {
+                    found = z;
+                    break;
+                }
+            }
+            if (found < 0) found = last;
+        }
+        if (!hit) {
+            // rounding put u * total past the lanes' boundaries: the last token with weight here
+            for (int z = c1 - 1; z >= c0; --z)
+                if (w(z) > 0.f) {
+                    found = z;
+                    break;
+                }
+        }
+        if (found >= 0) atomicMax(pick, found);
     }
     __syncthreads();
     int r = *pick;
     if (r < 0 && total > 0.f) {
-        // rounding left u * total past every boundary: the last token with weight
+        // rounding left u * total past every warp boundary: the last token with weight
         int lastp = -1;
-        for (int z = z1 - 1; z >= z0; --z)
-            if (w(z) > 0.f) {
-                lastp = z;
-                break;
-            }
+        for (int z = z1 - 1 - lane; z >= z0 && lastp < 0; z -= 32)
+            if (w(z) > 0.f) lastp = z;
         atomicMax(pick, lastp);
         __syncthreads();
         r = *pick;
@@ -184,21 +218,24 @@ __global__ void __launch_bounds__(SNT) verify_sample_kernel(
     const float inv_td = 1.f / temp[0], inv_tv = 1.f / temp[1];
     const int* prop = proposal + (size_t)s * (B - 1);
     const float* u = u_verify + (size_t)s * B;
-    if (threadIdx.x == 0) {
-        int a = 0;
-        for (; a < B - 1; ++a) {
-            const int y = prop[a];
+    if (threadIdx.x < 32) {
+        // lane j decides proposal j (B - 1 <= 31); a = the number of leading accepts
+        const int j = threadIdx.x;
+        bool ok = false;
+        if (j < B - 1) {
+            const int y = prop[j];
             if (y < 0 || y >= V) {
                 atomicOr(err, ERR_TOKEN_RANGE);
-                break;
+            } else {
+                const float2 ts = tstat[s * B + j], ds = dstat[s * B + j + 1];
+                const float p = expf((logits[(size_t)(s * B + j) * V + y] - ts.x) * inv_tv) / ts.y;
+                const float q = expf((dlogits[(size_t)(s * B + j + 1) * V + y] - ds.x) * inv_td) / ds.y;
+                const float ratio = q > 0.f ? fminf(1.f, p / q) : 1.f;
+                ok = clamp_u(u[j]) < ratio;
             }
-            const float2 ts = tstat[s * B + a], ds = dstat[s * B + a + 1];
-            const float p = expf((logits[(size_t)(s * B + a) * V + y] - ts.x) * inv_tv) / ts.y;
-            const float q = expf((dlogits[(size_t)(s * B + a + 1) * V + y] - ds.x) * inv_td) / ds.y;
-            const float ratio = q > 0.f ? fminf(1.f, p / q) : 1.f;
-            if (!(clamp_u(u[a]) < ratio)) break;
         }
-        a_s = a;
+        const unsigned rej = __ballot_sync(0xffffffffu, !ok);  // lanes >= B-1 count as rejections
+        if (j == 0) a_s = __ffs(rej) - 1;
     }
     __syncthreads();
     const int a = a_s;
