@@ -399,6 +399,10 @@ def run_ours(args, rank, world, local):
     timed_rounds(sess, props_dev, acc_dev, bon_dev, drafts_dev, W, K)
     sess.set_profiling(False)
     prof = sess.profile()
+    # one warm prefill of the same prompts (time to first token, CUDA events inside the library)
+    p0 = sess.stats().prefill_ms
+    sess.prefill(prompts)
+    prefill_ms = sess.stats().prefill_ms - p0
     sess.close()
 
     hbm, tf, tf_sus, peak_src = measured_peaks()
@@ -432,6 +436,8 @@ def run_ours(args, rank, world, local):
                       "frac": round_bytes / (h["ms_per_step"] * 1e-3) / 1e9 / hbm},
         "kernels": kernels, "gpu_launches": int(head_launches), "launches_per_round": launches_per_round,
         "clocks": clocks, "setup_s": {"init": t_init, "stream": t_stream},
+        "prefill": {"ms": prefill_ms, "tokens": int(sum(w.prompt_lens)),
+                    "tokens_per_s": sum(w.prompt_lens) / (prefill_ms * 1e-3) if prefill_ms > 0 else None},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
