@@ -280,7 +280,9 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
     float* rstd_s = reinterpret_cast<float*>(tmem_slot + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nt = blockIdx.x, mt = blockIdx.y, split = blockIdx.z;
+    // token tiles run fastest: the token tiles of one weight tile run together and share
+    // its L2 copy (the weight stream is read from DRAM once)
+    const int mt = blockIdx.x, nt = blockIdx.y, split = blockIdx.z;
     const int n0 = nt * BN, m0 = mt * MT;
     const int KB = (a.K + BK - 1) / BK;
     const int kb0 = split * a.kb_per_split;
@@ -829,7 +831,7 @@ bool launch_tc(const Launch& L, const CUtensorMap& mw, const CUtensorMap& mx, Tc
     if (!fits(1)) return false;
     a.kb_per_split = (KB + splits - 1) / splits;
     a.splits = (KB + a.kb_per_split - 1) / a.kb_per_split;
-    dim3 grid(a.n_tiles, m_tiles, a.splits);
+    dim3 grid(m_tiles, a.n_tiles, a.splits);
     launch_k(L, tc_gemm_kernel<MT, STAGES, NORM_A>, grid, dim3(THREADS), (size_t)S::TOTAL, a.splits, mw, mx, a);
     return true;
 }
