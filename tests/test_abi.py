@@ -114,4 +114,6 @@ def test_null_arguments(lib):
     assert lib.dflash_prefill(None, 1, None, None, None) == dfl.DFLASH_E_INVAL
     assert lib.dflash_draft_block(None, None) == dfl.DFLASH_E_INVAL
     assert lib.dflash_verify(None, None, None, None) == dfl.DFLASH_E_INVAL
+    assert lib.dflash_draft_block_sampled(None, 1.0, None, None) == dfl.DFLASH_E_INVAL
+    assert lib.dflash_verify_sampled(None, 1.0, None, None, None, None) == dfl.DFLASH_E_INVAL
     lib.dflash_destroy(None)
