@@ -15,6 +15,9 @@ metrics  acceptance length, cycle latency, speedup, memory accounting,
 sampling rounds at temperature T > 0: draft laws, proposals drawn by
          inverse CDF from caller-supplied uniforms, acceptance min(1, p/q),
          residual resampling, bonus draw.
+training the drafter's training forward (loss value): features of the clean
+         sequence, anchor blocks with their legal context, the packed
+         block-sparse pass, position-weighted cross-entropy (eq. 12).
 
 Pins (checked by ``tests/test_oracle_*.py`` against the pages and the
 mathematics, not against this code):
@@ -35,11 +38,15 @@ mathematics, not against this code):
   frequencies, eq. 7's two forms of the residual mass and the review's worked
   totals, eq. 8 (the emitted token has the target's law) by seeded Monte
   Carlo, which also rejects resampling from the target on rejection, and the
-  T -> 0 limit equal to the greedy round.
+  T -> 0 limit equal to the greedy round;
+* training: the packed block-sparse pass equals one pass per anchor, a block
+  equals the inference draft pass with the same context and anchor token, no
+  block sees a token at or after its anchor (or another block), the review's
+  lambda table and final weight, and the closed-form loss of a uniform drafter.
 
 Parity unpinned: the drafter's numerical output as a whole.  No trained draft
 weights exist here, so nothing outside this code fixes what a random-init
 drafter should propose beyond the structural pins above (context injection,
 bidirectional attention, cache reuse and immutability).
 """
-from . import metrics, model, sampling, spec  # noqa: F401
+from . import metrics, model, sampling, spec, training  # noqa: F401
