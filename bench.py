@@ -109,6 +109,22 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def job_throughput(tokens_local: float, seconds_local: float, world: int):
+    """Whole-job throughput of independent replicas: the tokens all ranks produced over
+    the slowest rank's time (sum and max over the process group; none when world == 1).
+    Returns (tokens per second, slowest time in seconds)."""
+    if world == 1:
+        return tokens_local / seconds_local, seconds_local
+    import torch
+    dist = torch.distributed
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds_local], dtype=torch.float64, device=dev)
+    n = torch.tensor([tokens_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(n.item()) / float(t.item()), float(t.item())
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -317,13 +333,6 @@ def run_ours(args, rank, world, local):
         if world > 1:
             torch.distributed.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
-
     drafts_dev = torch.zeros((b, max(B - 1, 1)), dtype=torch.int32, device="cuda")
     per_tau = {}
     launches_per_round = None
@@ -351,13 +360,14 @@ def run_ours(args, rank, world, local):
         launches = sess.stats().kernel_launches - l0
         got = acc_dev.cpu().numpy()[W:]
         tau = float(np.mean(got + 1))
-        ms_step = max_over_ranks(total_ms / K)
+        job_tps, job_s = job_throughput(float((got + 1).sum()), total_ms * 1e-3, world)
+        ms_step = job_s * 1e3 / K
         td = statistics.median(p[0] for p in per)
         tv = statistics.median(p[1] for p in per)
         per_tau[tau_name] = {
             "tau_planned": float(np.mean(accs[W:] + 1)), "tau": tau, "ms_per_step": ms_step,
             "t_draft_ms": td, "t_verify_ms": tv,
-            "tokens_per_s": world * b * tau / (ms_step * 1e-3),
+            "tokens_per_s": job_tps,
         }
         if headline:
             launches_per_round = launches / K
@@ -382,8 +392,8 @@ def run_ours(args, rank, world, local):
         sess.draft_block(drafts_h)
         sess.verify(host_props[r], acc_h, bon_h)
         emitted += int(acc_h.sum()) + b
-    e2e_s = max_over_ranks(time.perf_counter() - t0)
-    e2e = {"value": world * emitted / e2e_s, "unit": "tokens/s",
+    e2e_tps, e2e_s = job_throughput(float(emitted), time.perf_counter() - t0, world)
+    e2e = {"value": e2e_tps, "unit": "tokens/s",
            "h2d_bytes_per_step": int(b * max(B - 1, 0) * 4),
            "d2h_bytes_per_step": int(b * max(B - 1, 0) * 4 + 2 * b * 4),
            "ms_per_step": 1e3 * e2e_s / K}
