@@ -121,3 +121,36 @@ def test_zero_temperature_limit_is_the_greedy_round():
         rs = sp.verify_sampled(m, st_s, y, q, 1e-9, rng.random(B1), float(rng.random()))
         assert (rs.accepted, rs.bonus) == (rg.accepted, rg.bonus)
         assert st_s.committed == st_g.committed
+
+
+def test_round_emits_its_first_token_with_the_target_law():
+    """Whole round (draft, acceptance, residual): on a toy model the first token
+    a sampled round emits has the target's law after the anchor (eq. 8 applied
+    to the round), whatever the drafter proposes."""
+    w = configs.get("tiny_f32").with_(name="toy_sampling", vocab=16, d_model=32, n_heads=2, n_kv_heads=1,
+                                      head_dim=16, ffn=64, target_layers=2, draft_layers=1, ctx_layer_ids=(0, 1),
+                                      block_size=4, prompt_lens=(6,), weight_std=0.5)
+    m = om.Model(w)
+    T = 1.0
+    st0 = spec.prefill(m, synth.prompts(w)[0])
+    # the target's law of the token after the anchor
+    lg, _ = m.target_forward([st0.anchor], st0.tcache.copy())
+    p0 = sp.softmax_t(lg[0], T)
+    rng = np.random.default_rng(21)
+    n = 6000
+    counts = np.zeros(w.vocab)
+    B1 = w.block_size - 1
+    for _ in range(n):
+        st = copy.deepcopy(st0)
+        y, q, _ = sp.draft_sampled(m, st, T, rng.random(B1))
+        rd = sp.verify_sampled(m, st, y, q, T, rng.random(B1), float(rng.random()))
+        first = int(y[0]) if rd.accepted >= 1 else rd.bonus
+        counts[first] += 1
+    assert np.abs(counts / n - p0).max() < 5 * np.sqrt(0.25 / n)
+
+
+def test_round_pin_catches_resampling_from_the_target(monkeypatch):
+    """The same whole-round check fails when a rejection draws from p instead of the residual."""
+    monkeypatch.setattr(sp, "residual", lambda p, q: (np.asarray(p, np.float64), 1.0))
+    with pytest.raises(AssertionError):
+        test_round_emits_its_first_token_with_the_target_law()
