@@ -9,7 +9,7 @@ calls raise.
 The functions carry the C names:
 
     dflash_init, dflash_prefill, dflash_draft_block, dflash_verify,
-    dflash_draft_block_sampled, dflash_verify_sampled,
+    dflash_draft_block_sampled, dflash_verify_sampled, dflash_train_forward,
     dflash_generate, dflash_inspect, dflash_destroy, dflash_last_error
 
 ``Session`` wraps them for tests and the benchmark.
@@ -81,7 +81,7 @@ class dflash_profile_entry(ctypes.Structure):
 
 
 EXPORTS = ("dflash_init", "dflash_prefill", "dflash_draft_block", "dflash_verify", "dflash_draft_block_sampled",
-           "dflash_verify_sampled", "dflash_generate",
+           "dflash_verify_sampled", "dflash_train_forward", "dflash_generate",
            "dflash_inspect", "dflash_set_profiling", "dflash_destroy", "dflash_last_error")
 
 _lib = None
@@ -109,6 +109,7 @@ def load(build_if_missing: bool = False):
     lib.dflash_verify.argtypes = [P, P, P, P]
     lib.dflash_draft_block_sampled.argtypes = [P, ctypes.c_float, P, P]
     lib.dflash_verify_sampled.argtypes = [P, ctypes.c_float, P, P, P, P]
+    lib.dflash_train_forward.argtypes = [P, I32, P, I32, P, ctypes.c_float, P]
     lib.dflash_generate.argtypes = [P, I32, P, P, I32, P, P, ctypes.POINTER(dflash_stats)]
     lib.dflash_inspect.argtypes = [P, I32, I32, I32, P, SZ, ctypes.POINTER(SZ)]
     lib.dflash_set_profiling.argtypes = [P, I32]
@@ -116,7 +117,7 @@ def load(build_if_missing: bool = False):
     lib.dflash_last_error.argtypes = [P]
     lib.dflash_last_error.restype = ctypes.c_char_p
     for f in ("dflash_init", "dflash_prefill", "dflash_draft_block", "dflash_verify", "dflash_draft_block_sampled",
-              "dflash_verify_sampled", "dflash_generate",
+              "dflash_verify_sampled", "dflash_train_forward", "dflash_generate",
               "dflash_inspect", "dflash_set_profiling"):
         getattr(lib, f).restype = ctypes.c_int
     lib.dflash_destroy.restype = None

@@ -98,6 +98,7 @@ struct dflash_ctx {
     float* temp_pinned = nullptr;          // host staging of the two temperatures
     float temp_cur[2] = {-1.f, -1.f};      // values last written to temp_dev
     bool draft_sampled = false;
+    bool draft_logits_out = false;         // the draft pass also writes its logits to dlogits
     void* feat = nullptr;
     float* ss_x = nullptr;   // [ss_tiles][R]: per-128-column sums of squares of x rows (fused norms)
     float* ss_fc = nullptr;  // same for fcout
@@ -708,7 +709,8 @@ struct Pass {
         layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, false, keys, B);
         join_append();  // (already joined by the last layer's attention; kept for clarity)
         // drafts[s][j] = argmax of row s*B + 1 + j
-        head(0, b * B, c->draft_norm, c->drafts, c->keep_draft, B, sampled ? c->dlogits : nullptr);
+        head(0, b * B, c->draft_norm, c->drafts, c->keep_draft, B,
+             (sampled || c->draft_logits_out) ? c->dlogits : nullptr);
         if (sampled)  // drafts[s][j] = draw from q of row s*B + 1 + j (replaces the argmax)
             timed(c, DFLASH_K_ARGMAX, (double)b * (B - 1) * c->V * 8, 0, [&] {
                 draft_sample(L, c->dlogits, c->V, b, B, c->temp_dev, c->u_draft, c->dstat, c->drafts);
@@ -1229,6 +1231,86 @@ dflash_status dflash_verify_sampled(dflash_ctx* c, float temperature, const int3
     } else if (h2) {
         if ((s = check_device(c))) return s;
     }
+    return DFLASH_OK;
+}
+
+dflash_status dflash_train_forward(dflash_ctx* c, int32_t n_tokens, const int32_t* tokens, int32_t n_anchors,
+                                   const int32_t* anchors, float lambda, float* loss) {
+    if (!c) return DFLASH_E_INVAL;
+    if (!tokens || !anchors || !loss || n_anchors < 1) return c->fail(DFLASH_E_INVAL, "NULL argument or no anchors");
+    const int B = c->B, m = n_anchors;
+    if (B < 2) return c->fail(DFLASH_E_INVAL, "block size 1 predicts no token");
+    if (!(lambda > 0.f) || !std::isfinite(lambda)) return c->fail(DFLASH_E_INVAL, "lambda %g is not positive", lambda);
+    if (m + 1 > c->cfg.max_batch)
+        return c->fail(DFLASH_E_CAPACITY, "%d anchors need max_batch >= %d", m, m + 1);
+    for (int i = 0; i < m; ++i)
+        if (anchors[i] < 1 || anchors[i] + B - 1 >= n_tokens)
+            return c->fail(DFLASH_E_INVAL, "anchor %d = %d outside [1, %d]", i, anchors[i], n_tokens - B);
+    // 1. the target's features of the clean sequence: its context K/V in slot 0
+    int first = 0;
+    dflash_status s = dflash_prefill(c, 1, &n_tokens, tokens, &first);
+    if (s) return s;
+    // 2. slot i+1 shares slot 0's pages below its anchor's page and owns the rest
+    const int pps = c->kv.pages_per_seq;
+    const size_t pages = (size_t)c->cfg.max_batch * pps;
+    std::vector<int> pt(pages), ident(pages);
+    for (size_t i = 0; i < pages; ++i) pt[i] = ident[i] = (int)i;
+    for (int i = 0; i < m; ++i)
+        for (int t = 0; t < (anchors[i] >> PAGE_SHIFT); ++t) pt[(size_t)(i + 1) * pps + t] = t;
+    CUDA_TRY(c, cudaMemcpyAsync(c->page_table, pt.data(), pages * 4, cudaMemcpyHostToDevice, c->stream));
+    // 3. its own copy of the anchor's page (the context rows below the anchor in that page)
+    const size_t page_elems = (size_t)c->Hkv * PAGE_TOKENS * c->hd;
+    for (int l = 0; l < c->Ld; ++l)
+        for (int i = 0; i < m; ++i) {
+            const int p0 = anchors[i] >> PAGE_SHIFT;
+            const size_t src = (size_t)l * c->kv.layer_stride + (size_t)p0 * page_elems;
+            const size_t dst = (size_t)l * c->kv.layer_stride + ((size_t)(i + 1) * pps + p0) * page_elems;
+            CUDA_TRY(c, cudaMemcpyAsync((char*)c->dK + dst * c->esz, (char*)c->dK + src * c->esz, page_elems * c->esz,
+                                        cudaMemcpyDeviceToDevice, c->stream));
+            CUDA_TRY(c, cudaMemcpyAsync((char*)c->dV + dst * c->esz, (char*)c->dV + src * c->esz, page_elems * c->esz,
+                                        cudaMemcpyDeviceToDevice, c->stream));
+        }
+    // 4. one block per anchor: slot i+1 has length a_i and anchor token x[a_i]; labels x[a_i + k]
+    std::vector<int> nh(m + 1), ah(m + 1), labels((size_t)m * (B - 1));
+    nh[0] = n_tokens;
+    ah[0] = first;
+    for (int i = 0; i < m; ++i) {
+        nh[i + 1] = anchors[i];
+        ah[i + 1] = tokens[anchors[i]];
+        for (int k = 1; k < B; ++k) labels[(size_t)i * (B - 1) + k - 1] = tokens[anchors[i] + k];
+    }
+    CUDA_TRY(c, cudaMemcpyAsync(c->n, nh.data(), nh.size() * 4, cudaMemcpyHostToDevice, c->stream));
+    CUDA_TRY(c, cudaMemcpyAsync(c->anchor, ah.data(), ah.size() * 4, cudaMemcpyHostToDevice, c->stream));
+    CUDA_TRY(c, cudaMemcpyAsync(c->proposal, labels.data(), labels.size() * 4, cudaMemcpyHostToDevice, c->stream));
+    c->batch = m + 1;
+    c->n_upper = nh;
+    c->pending_append = false;
+    // 5. the drafter over every block at once, logits kept; 6. per-row cross-entropy
+    c->draft_logits_out = true;
+    if (c->cfg.dtype == DFLASH_DTYPE_BF16) Pass<bf16>{c}.draft();
+    else Pass<float>{c}.draft();
+    c->draft_logits_out = false;
+    {
+        Launch L = c->L();
+        row_nll(L, c->dlogits, c->V, B, 1, m, c->proposal, c->u_draft);
+    }
+    std::vector<float> nll((size_t)m * (B - 1));
+    CUDA_TRY(c, cudaMemcpyAsync(nll.data(), c->u_draft, nll.size() * 4, cudaMemcpyDeviceToHost, c->stream));
+    // 7. identity pages again; the session needs a new prefill before any round
+    CUDA_TRY(c, cudaMemcpyAsync(c->page_table, ident.data(), pages * 4, cudaMemcpyHostToDevice, c->stream));
+    CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+    c->batch = 0;
+    c->state = ST_EMPTY;
+    if ((s = launch_check(c))) return s;
+    if ((s = check_device(c))) return s;
+    // eq. 12: mean over anchors of the exp(-(k-1)/lambda)-weighted sum, in a fixed order
+    double total = 0.0;
+    for (int i = 0; i < m; ++i) {
+        double blk = 0.0;
+        for (int k = 1; k < B; ++k) blk += exp(-(double)(k - 1) / (double)lambda) * (double)nll[(size_t)i * (B - 1) + k - 1];
+        total += blk;
+    }
+    *loss = (float)(total / m);
     return DFLASH_OK;
 }
 

@@ -264,6 +264,29 @@ __global__ void __launch_bounds__(SNT) verify_sample_kernel(
     }
 }
 
+// Training loss rows: for sequence slots first .. first + n - 1 and block rows k = 1 .. B-1,
+// out[i*(B-1) + k-1] = -log softmax(logits row)[label] = max + log sum exp(l - max) - l[label].
+__global__ void __launch_bounds__(SNT) row_nll_kernel(const float* __restrict__ logits, int V, int B, int first,
+                                                      const int* __restrict__ labels, float* __restrict__ out,
+                                                      uint32_t* err) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float red[32];
+    const int k = blockIdx.x, i = k / (B - 1), j = k % (B - 1) + 1;
+    const float* l = logits + (size_t)((first + i) * B + j) * V;
+    float m, sum;
+    row_stats(l, V, 1.f, red, m, sum);
+    if (threadIdx.x == 0) {
+        const int y = labels[k];
+        if (y < 0 || y >= V) {
+            atomicOr(err, ERR_TOKEN_RANGE);
+            out[k] = 0.f;
+        } else {
+            out[k] = m + logf(sum) - l[y];
+        }
+    }
+}
+
 }  // namespace
 
 void draft_sample(const Launch& L, const float* dlogits, int V, int batch, int B, const float* temp,
@@ -280,6 +303,12 @@ void verify_sample(const Launch& L, const float* logits, const float* dlogits, i
     launch_k(L, target_stats_kernel, dim3(batch * B), dim3(SNT), 0, 1, logits, V, temp, tstat);
     launch_k(L, verify_sample_kernel, dim3(batch), dim3(SNT), 0, 1, logits, dlogits, V, B, temp, proposal, u_verify,
              (const float2*)tstat, dstat, n, anchor, accepted, bonus, ctx_row_seq, ctx_row_pos, L.err);
+}
+
+void row_nll(const Launch& L, const float* logits, int V, int B, int first_seq, int n_seqs, const int* labels,
+             float* out) {
+    if (n_seqs <= 0 || B < 2) return;
+    launch_k(L, row_nll_kernel, dim3(n_seqs * (B - 1)), dim3(SNT), 0, 1, logits, V, B, first_seq, labels, out, L.err);
 }
 
 }  // namespace dfl

@@ -176,6 +176,17 @@ class Session:
                                                         _ptr(accepted), _ptr(emitted)))
         return accepted, emitted
 
+    def train_forward(self, tokens, anchors, lam: float) -> float:
+        """The drafter's position-weighted training loss over one clean sequence
+        (one block per anchor).  Leaves the session empty."""
+        toks = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        anc = np.ascontiguousarray(np.asarray(anchors, dtype=np.int32))
+        loss = np.zeros(1, dtype=np.float32)
+        _check(self.ctx, self.lib.dflash_train_forward(self.ctx, len(toks), _ptr(toks), len(anc), _ptr(anc),
+                                                       float(lam), _ptr(loss)))
+        self.batch = 0
+        return float(loss[0])
+
     def generate(self, prompts: Sequence[np.ndarray], max_new_tokens: int):
         lens = np.array([len(p) for p in prompts], dtype=np.int32)
         toks = np.ascontiguousarray(np.concatenate([np.asarray(p, dtype=np.int32) for p in prompts]))

@@ -237,6 +237,22 @@ dflash_status dflash_draft_block_sampled(dflash_ctx* ctx, float temperature, con
 dflash_status dflash_verify_sampled(dflash_ctx* ctx, float temperature, const int32_t* draft_tokens,
                                     const float* u_verify, int32_t* accepted, int32_t* emitted);
 
+/* The drafter's training forward, loss value only ([review] §6 eq. 12 and
+ * Algorithm 2; [digest] Training §4.2).  The target runs once, causally, over
+ * the clean sequence tokens[0..n_tokens); for each anchor a the block
+ * [tokens[a], MASK x (B-1)] at positions a .. a+B-1 attends to the fused
+ * target features of positions < a and to itself; the loss is the mean over
+ * anchors of sum_{k=1}^{B-1} exp(-(k-1)/lambda) * -log q_k(tokens[a+k]).
+ * All blocks run in one drafter pass: block i uses sequence slot i+1, whose
+ * page table shares slot 0's context pages below its anchor's page.
+ * tokens: host [n_tokens]; anchors: host [n_anchors], each in [1, n_tokens-B];
+ * loss: host float.  Needs B >= 2, n_anchors + 1 <= max_batch and
+ * n_tokens + B <= max_seq_len.  Leaves the session empty (prefill before the
+ * next round).  Errors: E_INVAL (NULL, anchor range, lambda <= 0, B < 2),
+ * E_CAPACITY, E_DEVICE_CHECK, E_CUDA. */
+dflash_status dflash_train_forward(dflash_ctx* ctx, int32_t n_tokens, const int32_t* tokens, int32_t n_anchors,
+                                   const int32_t* anchors, float lambda, float* loss);
+
 /* Greedy speculative generation ([digest] greedy decoding-round pseudocode):
  * prefill, then rounds of draft_block + verify until every sequence has
  * max_new_tokens tokens (the first token counts); each sequence's output is
