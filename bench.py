@@ -303,6 +303,42 @@ def run_sampled(args, local):
                    "proposals": "the drafter's own, drawn at T; uniforms from a seeded device generator"}}))
 
 
+def run_train(args, local):
+    """The drafter's training forward (dflash_train_forward): one causal target pass over
+    the workload's first prompt as the clean sequence, then one drafter pass over M anchor
+    blocks (evenly spaced) and the position-weighted loss; CUDA-event time per call."""
+    import numpy as np
+    import torch
+
+    import synth
+    from block_diffusion_speculative_ctx_gb300 import Session, build as dbuild
+
+    torch.cuda.set_device(local)
+    dbuild.build()
+    w = workload_of(args)
+    B, M = w.block_size, args.train_forward
+    x = np.asarray(synth.prompts(w)[0], dtype=np.int64)
+    anchors = np.linspace(1, len(x) - B, M).astype(np.int64)
+    lam = 7.0 if B == 16 else 5.0 if B == 10 else 4.0
+    sess = Session(w, max_batch=M + 1, max_seq_len=len(x) + 2 * B)
+    for _ in range(args.warmup):
+        loss = sess.train_forward(x, anchors, lam)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        loss = sess.train_forward(x, anchors, lam)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    sess.close()
+    print(json.dumps({
+        "metric": "drafter training forward (loss value) latency and predicted tokens/s, one GB300",
+        "value": M * (B - 1) / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "dtype": w.dtype, "data": "synthetic", "loss": loss,
+        "config": {"workload": w.name, "sequence": len(x), "anchors": M, "block": B, "lambda": lam}}))
+
+
 def run_ours(args, rank, world, local):
     import numpy as np
     import torch
@@ -566,6 +602,8 @@ def main():
     ap.add_argument("--block", type=int, default=0, help="block size B (default: the workload's, 16)")
     ap.add_argument("--temperature", type=float, default=0.0,
                     help="T > 0: time sampled rounds (speculative rejection sampling) instead of greedy ones")
+    ap.add_argument("--train-forward", type=int, default=0, metavar="M",
+                    help="time the drafter's training forward with M anchor blocks instead of rounds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ncu-target", action="store_true",
@@ -583,6 +621,9 @@ def main():
         return
     if args.temperature > 0:
         run_sampled(args, local)
+        return
+    if args.train_forward > 0:
+        run_train(args, local)
         return
     if world > 1:
         import torch
