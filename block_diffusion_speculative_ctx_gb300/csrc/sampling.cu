@@ -5,7 +5,7 @@
 // "Sampling rule".
 //
 // Laws are softmax(logits / T) of fp32 logit rows: q from the draft head's
-// rows 1..B-1, p from the verify head's rows 0..B-1 (p_j judges the proposal
+// rows 1..B-1, p from the verify head's rows 0..B-1 (p_j decides the proposal
 // at block row j + 1).  Every draw is an inverse-CDF lookup of a caller-supplied
 // uniform u in [0, 1): the lowest token z whose cumulative weight exceeds
 // u * total.  One CTA handles one row (draws) or one sequence (acceptance and

@@ -16,7 +16,7 @@ Readings where the pages leave the step open:
 - laws: q_j = softmax(draft logits of block row j / T) for the mask rows
   j = 1..B-1; p_j = softmax(verify logits of block row j / T), the target's
   law for the token after block row j (so proposal j, block row j + 1, is
-  judged under p_j); top-p / top-k are not applied;
+  accepted or rejected under p_j); top-p / top-k are not applied;
 - every draw is an inverse-CDF lookup with a caller-supplied uniform
   u in [0, 1): the lowest index z whose cumulative weight exceeds u times the
   total weight (the method's random numbers are inputs, so both sides of a
