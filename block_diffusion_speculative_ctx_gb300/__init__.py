@@ -8,7 +8,8 @@ calls raise.
 
 The functions carry the C names:
 
-    dflash_init, dflash_prefill, dflash_draft_block, dflash_verify,
+    dflash_init, dflash_prefill, dflash_set_block_size, dflash_block_size,
+    dflash_draft_block, dflash_verify,
     dflash_draft_block_sampled, dflash_verify_sampled, dflash_train_forward,
     dflash_generate, dflash_inspect, dflash_destroy, dflash_last_error
 
@@ -80,7 +81,7 @@ class dflash_profile_entry(ctypes.Structure):
                 ("flops", ctypes.c_double)]
 
 
-EXPORTS = ("dflash_init", "dflash_prefill", "dflash_draft_block", "dflash_verify", "dflash_draft_block_sampled",
+EXPORTS = ("dflash_init", "dflash_prefill", "dflash_set_block_size", "dflash_block_size", "dflash_draft_block", "dflash_verify", "dflash_draft_block_sampled",
            "dflash_verify_sampled", "dflash_train_forward", "dflash_generate",
            "dflash_inspect", "dflash_set_profiling", "dflash_destroy", "dflash_last_error")
 
@@ -113,12 +114,15 @@ def load(build_if_missing: bool = False):
     lib.dflash_generate.argtypes = [P, I32, P, P, I32, P, P, ctypes.POINTER(dflash_stats)]
     lib.dflash_inspect.argtypes = [P, I32, I32, I32, P, SZ, ctypes.POINTER(SZ)]
     lib.dflash_set_profiling.argtypes = [P, I32]
+    lib.dflash_set_block_size.argtypes = [P, I32]
+    lib.dflash_block_size.argtypes = [P]
+    lib.dflash_block_size.restype = I32
     lib.dflash_destroy.argtypes = [P]
     lib.dflash_last_error.argtypes = [P]
     lib.dflash_last_error.restype = ctypes.c_char_p
     for f in ("dflash_init", "dflash_prefill", "dflash_draft_block", "dflash_verify", "dflash_draft_block_sampled",
               "dflash_verify_sampled", "dflash_train_forward", "dflash_generate",
-              "dflash_inspect", "dflash_set_profiling"):
+              "dflash_inspect", "dflash_set_profiling", "dflash_set_block_size"):
         getattr(lib, f).restype = ctypes.c_int
     lib.dflash_destroy.restype = None
     _lib = lib

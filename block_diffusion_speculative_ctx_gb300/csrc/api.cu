@@ -61,6 +61,8 @@ struct dflash_ctx {
     size_t esz = 4;  // element size of the storage type
 
     int d, H, Hkv, hd, F, V, Lt, Ld, B, k, qd, kvd, qkv_n, max_seq;
+    int Bmax = 0;      // configured block size: every round buffer is sized for it
+    int append_B = 0;  // block size of the verify whose accepted rows await the context append
     int ctx_slot[64];  // target layer -> index in ctx_layer_ids or -1
 
     std::vector<LayerW> tl, dl;
@@ -150,7 +152,7 @@ struct dflash_ctx {
     // verify pass, captured on `cap_stream` and replayed on `stream`
     struct GraphSlot {
         cudaGraphExec_t exec = nullptr;
-        int batch = -1;
+        long long key = -1;  // (batch, block size, block size of the pending append)
         long long kernels = 0;
         int eager_runs = 0;
     };
@@ -685,11 +687,11 @@ struct Pass {
                     cudaStreamWaitEvent(c->side_stream, c->ctx_ev[c->Ld], 0) != cudaSuccess)
                     c->launch_failed = true;
                 c->stream = c->side_stream;
-                append_context(b * B, c->ctx_row_seq, c->ctx_row_pos, c->ctx_ev.data());
+                append_context(b * c->append_B, c->ctx_row_seq, c->ctx_row_pos, c->ctx_ev.data());
                 c->stream = main;
                 c->append_forked = true;
             } else {
-                append_context(b * B, c->ctx_row_seq, c->ctx_row_pos);
+                append_context(b * c->append_B, c->ctx_row_seq, c->ctx_row_pos);
             }
             c->pending_append = false;
         }
@@ -751,6 +753,7 @@ struct Pass {
             });
         }
         c->pending_append = true;
+        c->append_B = B;
     }
 };
 
@@ -794,15 +797,16 @@ dflash_status run_pass(dflash_ctx* c, dflash_ctx::GraphSlot& g, F&& pass) {
         pass();
         return launch_check(c);
     }
-    if (g.exec && g.batch == c->batch) {
+    const long long key = ((long long)c->batch << 16) | (c->B << 8) | (c->pending_append ? c->append_B : 0);
+    if (g.exec && g.key == key) {
         CUDA_TRY(c, cudaGraphLaunch(g.exec, c->stream));
         c->launches += g.kernels;
         // host-side effects of the pass
         return DFLASH_OK;
     }
-    if (g.batch != c->batch) {
+    if (g.key != key) {
         reset_graph(g);
-        g.batch = c->batch;
+        g.key = key;
     }
     if (g.eager_runs < 1) {
         ++g.eager_runs;
@@ -854,6 +858,7 @@ dflash_status do_verify(dflash_ctx* c, bool sampled = false) {
     });
     if (s != DFLASH_OK) return s;
     c->pending_append = true;
+    c->append_B = c->B;
     for (int i = 0; i < c->batch; ++i) c->n_upper[i] += c->B;
     return DFLASH_OK;
 }
@@ -944,6 +949,7 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     c->Lt = cfg->target_layers;
     c->Ld = cfg->draft_layers;
     c->B = cfg->block_size;
+    c->Bmax = cfg->block_size;
     c->k = cfg->n_ctx_layers;
     c->qd = c->H * c->hd;
     c->kvd = c->Hkv * c->hd;
@@ -1023,7 +1029,7 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
         }
     }
     // round buffers
-    const int rb = cfg->max_batch * c->B;
+    const int rb = cfg->max_batch * c->Bmax;
     c->R = std::max(rb, PREFILL_CHUNK);
     const size_t R = c->R;
     ALLOC(c->x, R * d * 4);
@@ -1060,13 +1066,13 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     ALLOC(c->ctx_row_pos, (size_t)rb * 4);
     ALLOC(c->n, (size_t)cfg->max_batch * 4);
     ALLOC(c->anchor, (size_t)cfg->max_batch * 4);
-    ALLOC(c->proposal, (size_t)cfg->max_batch * c->B * 4);
+    ALLOC(c->proposal, (size_t)cfg->max_batch * c->Bmax * 4);
     ALLOC(c->posterior, (size_t)rb * 4);
     ALLOC(c->argbuf, (size_t)rb * 4);
     ALLOC(c->keys, (size_t)std::max(rb, cfg->max_batch) * 8);
     ALLOC(c->accepted, (size_t)cfg->max_batch * 4);
     ALLOC(c->bonus, (size_t)cfg->max_batch * 4);
-    ALLOC(c->drafts, (size_t)cfg->max_batch * c->B * 4);
+    ALLOC(c->drafts, (size_t)cfg->max_batch * c->Bmax * 4);
     ALLOC(c->errw, 16);
     ALLOC(c->attn_ws, ATTN_WS_BYTES);
     ALLOC(c->gemm_ws, GEMM_WS_BYTES);
@@ -1154,6 +1160,17 @@ dflash_status dflash_prefill(dflash_ctx* c, int32_t batch, const int32_t* lens, 
     c->state = ST_READY;
     return DFLASH_OK;
 }
+
+dflash_status dflash_set_block_size(dflash_ctx* c, int32_t block_size) {
+    if (!c) return DFLASH_E_INVAL;
+    if (block_size < 1 || block_size > c->Bmax)
+        return c->fail(DFLASH_E_INVAL, "block size %d outside [1, %d] (the configured block size)", block_size, c->Bmax);
+    if (c->state == ST_DRAFTED) return c->fail(DFLASH_E_STATE, "set_block_size between draft_block and verify");
+    c->B = block_size;
+    return DFLASH_OK;
+}
+
+int32_t dflash_block_size(const dflash_ctx* c) { return c ? c->B : -1; }
 
 dflash_status dflash_draft_block(dflash_ctx* c, int32_t* draft_tokens) {
     if (!c) return DFLASH_E_INVAL;

@@ -135,6 +135,11 @@ class Session:
         self.batch = len(prompts)
         return first
 
+    def set_block_size(self, B: int):
+        """Block size of the following rounds, 1 <= B <= the configured one."""
+        _check(self.ctx, self.lib.dflash_set_block_size(self.ctx, int(B)))
+        self.B = int(self.lib.dflash_block_size(self.ctx))
+
     def draft_block(self, out=None):
         """Draft tokens [batch, B-1]; ``out`` may be a numpy array or a device tensor."""
         if out is None:

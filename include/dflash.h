@@ -180,6 +180,24 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
 dflash_status dflash_prefill(dflash_ctx* ctx, int32_t batch, const int32_t* prompt_lens,
                              const int32_t* prompt_tokens, int32_t* first_tokens);
 
+/* Set the block size B of the following rounds to block_size, between 1 and
+ * the configured block size (the drafter's training block).  A drafter trained
+ * at one block size still drafts well at a smaller one, and a smaller block
+ * is cheaper to verify when the target is compute-bound at large batch
+ * ("DFlash" wiki, Ablations: block size; [digest] Pitfalls, on §5.5.4 and tab. 8).
+ * Weights, caches and committed lengths are unchanged; a pending context
+ * append keeps the block size of the verify that produced it.  The sizes of
+ * every round array (draft_tokens [batch, B-1], the sampled calls' uniforms,
+ * dflash_inspect's per-row items) follow the new B from the next draft on,
+ * and dflash_inspect's kept rows of earlier rounds are read with the current B.
+ * Allowed before a prefill and between a verify and the next draft.
+ * Errors: E_INVAL (ctx NULL or block_size outside [1, configured B]),
+ * E_STATE (a draft awaits its verify). */
+dflash_status dflash_set_block_size(dflash_ctx* ctx, int32_t block_size);
+
+/* The block size of the next round (-1 for a NULL ctx). */
+int32_t dflash_block_size(const dflash_ctx* ctx);
+
 /* One drafting pass ([digest] Inference steps 2-3 and the draft-layer
  * pseudocode; [review] §5.1 eq. 10).  First appends the context features of
  * the anchor and accepted drafts of the previous verify (a_i + 1 rows per

@@ -19,6 +19,13 @@ Algorithm 1):
 5. keep target cache entries and context features only for the anchor and the
    accepted drafts; the bonus becomes the next anchor;
 6. stop once max_new_tokens are produced and cut the output to that length.
+
+A round may run with a smaller block than the drafter was trained with
+(``at_block_size``): the "DFlash" wiki (Ablations, block size) and the paper
+digest's Pitfalls (on §5.5.4 and tab. 8) report that a drafter trained at 16
+still drafts at 8, and suggest a smaller block when verification is
+compute-bound.  Reading: the same weights, B' rows [anchor, MASK x (B'-1)] at
+positions n .. n+B'-1; nothing else changes.
 """
 from __future__ import annotations
 
@@ -87,6 +94,14 @@ def prefill(model: Model, prompt) -> SeqState:
     return st
 
 
+def at_block_size(model: Model, B: int) -> Model:
+    """The same target and drafter with an inference block of B rows, 1 <= B <=
+    the configured (training) block size; the weights are shared, not copied."""
+    if not 1 <= B <= model.cfg.block_size:
+        raise ValueError(f"block size {B} outside [1, {model.cfg.block_size}]")
+    return Model(model.cfg.with_(block_size=B), weights=model.w, act_round=model.act_round)
+
+
 def draft(model: Model, st: SeqState):
     """Returns (drafts [B-1], logits [B, V])."""
     lg = model.draft_forward(st.anchor, st.dcache)
@@ -118,16 +133,22 @@ Proposer = Callable[[SeqState, np.ndarray], np.ndarray]
 
 
 def generate(model: Model, prompt, max_new_tokens: int, proposer: Optional[Proposer] = None,
-             keep_logits: bool = False, max_rounds: Optional[int] = None) -> SeqState:
+             keep_logits: bool = False, max_rounds: Optional[int] = None,
+             block_schedule: Optional[List[int]] = None) -> SeqState:
     """Speculative greedy decoding of one sequence.  ``proposer(state, drafts)``
-    may replace the drafter's tokens by any proposal of length B-1."""
+    may replace the drafter's tokens by any proposal of length B-1.
+    ``block_schedule``: block size of round r = block_schedule[r % len], each
+    at most the configured one (default: the configured block every round)."""
     st = prefill(model, prompt)
     while len(st.generated) < max_new_tokens:
         if max_rounds is not None and len(st.rounds) >= max_rounds:
             break
-        d, dl = draft(model, st)
+        m = model
+        if block_schedule:
+            m = at_block_size(model, int(block_schedule[len(st.rounds) % len(block_schedule)]))
+        d, dl = draft(m, st)
         prop = d if proposer is None else np.asarray(proposer(st, d), dtype=np.int64)
-        verify(model, st, prop, drafts=d, draft_logits=dl, keep_logits=keep_logits)
+        verify(m, st, prop, drafts=d, draft_logits=dl, keep_logits=keep_logits)
     st.generated = st.generated[:max_new_tokens]
     return st
 

@@ -116,4 +116,6 @@ def test_null_arguments(lib):
     assert lib.dflash_verify(None, None, None, None) == dfl.DFLASH_E_INVAL
     assert lib.dflash_draft_block_sampled(None, 1.0, None, None) == dfl.DFLASH_E_INVAL
     assert lib.dflash_verify_sampled(None, 1.0, None, None, None, None) == dfl.DFLASH_E_INVAL
+    assert lib.dflash_set_block_size(None, 4) == dfl.DFLASH_E_INVAL
+    assert lib.dflash_block_size(None) == -1
     lib.dflash_destroy(None)

@@ -54,9 +54,11 @@ def _rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), **wkw):
+def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), schedule=None, **wkw):
     """Prefill + `rounds` rounds on both sides; returns the number of
-    (sequence, round) pairs compared.  A bf16 sequence whose acceptance or bonus
+    (sequence, round) pairs compared.  `schedule`: block size of round r =
+    schedule[r % len] (dflash_set_block_size on the GPU, the oracle's
+    at_block_size view), default the configured block.  A bf16 sequence whose acceptance or bonus
     differs from the oracle's at an exempted near-tie stops being compared (its
     two streams now differ); the other sequences continue."""
     w = configs.get(name)
@@ -93,19 +95,24 @@ def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), **wkw):
         for r in range(rounds):
             if not any(alive):
                 break
+            Bt = schedule[r % len(schedule)] if schedule else w.block_size
+            mr = spec.at_block_size(m, Bt) if schedule else m
+            if schedule:
+                sess.set_block_size(Bt)
+                assert sess.B == Bt
             drafts = sess.draft_block()
-            dlog = sess.logits("draft") if w.block_size > 1 else None   # block 1 runs no drafter
+            dlog = sess.logits("draft") if Bt > 1 else None   # block 1 runs no drafter
             proposals = []
             for s, st in enumerate(states):
                 if not alive[s]:
-                    proposals.append(np.zeros(w.block_size - 1, np.int64))
+                    proposals.append(np.zeros(Bt - 1, np.int64))
                     continue
-                od, odl = spec.draft(m, st)
+                od, odl = spec.draft(mr, st)
                 if dlog is not None:
                     assert np.abs(dlog[s] - odl).max() <= ltol, f"round {r} seq {s} draft logits"
                     _tokens_match(drafts[s], odl[1:], bf16, near)      # mismatches only at near-ties
                 proposals.append(props[s](st, od))
-            prop = np.stack(proposals).astype(np.int32) if w.block_size > 1 else np.zeros((len(states), 1), np.int32)
+            prop = np.stack(proposals).astype(np.int32) if Bt > 1 else np.zeros((len(states), 1), np.int32)
             acc, bon = sess.verify(prop)
             vlog = sess.logits("verify")
             post = sess.posterior()
@@ -114,7 +121,7 @@ def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), **wkw):
                 if not alive[s]:
                     continue
                 n0 = st.committed
-                rd = spec.verify(m, st, prop[s][: w.block_size - 1], keep_logits=True)
+                rd = spec.verify(mr, st, prop[s][: Bt - 1], keep_logits=True)
                 assert np.abs(vlog[s] - rd.verify_logits).max() <= ltol, f"round {r} seq {s} verify logits"
                 _tokens_match(post[s], rd.verify_logits, bf16, near)
                 if acc[s] != rd.accepted or bon[s] != rd.bonus:
@@ -175,6 +182,34 @@ def test_small_bf16_block_sizes_8_and_10(block):
 def test_small_bf16_llama_block10_batch4():
     # GQA 4 with 10-row blocks: query groups of 40 vectors
     assert run_stepwise("small_bf16_llama", rounds=3, block_size=10) >= 6     # of 4 x 3
+
+
+@pytest.mark.parametrize("name", ["tiny_f32_b3", "small_bf16_llama"])
+def test_runtime_block_size_schedule(name):
+    # a session configured at its drafter's block runs rounds at smaller blocks
+    # (16 -> 8 -> 1 -> 12 -> 16 ...; the tiny drafter's 4 -> 2 -> 1 -> 3), sequences ragged
+    B = configs.get(name).block_size
+    sched = [B, B // 2, 1, 3 * B // 4]
+    assert run_stepwise(name, rounds=5, schedule=sched) >= 3 * 5 // 2
+
+
+def test_runtime_block_size_errors():
+    from block_diffusion_speculative_ctx_gb300 import DFlashError
+    w = configs.get("tiny_f32")
+    with _session(w, max_seq_len=96) as sess:
+        with pytest.raises(DFlashError, match="outside"):
+            sess.set_block_size(w.block_size + 1)
+        with pytest.raises(DFlashError, match="outside"):
+            sess.set_block_size(0)
+        sess.set_block_size(2)                            # before a prefill
+        sess.prefill(synth.prompts(w))
+        d = sess.draft_block()
+        assert d.shape == (1, 1)
+        with pytest.raises(DFlashError, match="between draft_block and verify"):
+            sess.set_block_size(3)
+        sess.verify(d)
+        sess.set_block_size(w.block_size)
+        assert sess.draft_block().shape == (1, w.block_size - 1)
 
 
 def test_block_size_one_is_plain_greedy():

@@ -86,20 +86,56 @@ def test_lossless_small_bf16(act_round):
     assert [r.accepted for r in st.rounds][:3] == [5, 6, 5]
 
 
+# ------------------------------------------------- runtime block size (B' <= B)
+def test_lossless_with_a_runtime_block_schedule():
+    """Rounds at blocks 7, 3, 1, 5 of a drafter configured at 7: output equals
+    plain greedy, each round accepts at most B'-1 drafts, and planted proposals
+    are accepted to min(tau, B') - 1."""
+    m, cfg = _model("tiny_f32", block_size=7)
+    p = synth.prompts(cfg)[0]
+    ar_long, _ = spec.ar_generate(m, p, 48 + 7)    # the last round's proposal may reach past token 48
+    ar = ar_long[:48]
+    sched = [7, 3, 1, 5]
+    st = spec.generate(m, p, 48, block_schedule=sched)
+    assert np.array_equal(np.array(st.generated), ar)
+    for i, r in enumerate(st.rounds):
+        assert len(r.posterior) == sched[i % 4] and 0 <= r.accepted <= sched[i % 4] - 1
+    taus = [6, 2, 4, 3, 7]
+    st = spec.generate(m, p, 48, proposer=spec.planted_proposer(ar_long, taus, cfg.vocab), block_schedule=sched)
+    assert np.array_equal(np.array(st.generated), ar)
+    assert [r.accepted for r in st.rounds] == [min(taus[i % 5], sched[i % 4]) - 1 for i in range(len(st.rounds))]
+
+
+def test_runtime_block_is_the_model_configured_at_that_block():
+    """The B' view of a B-configured model drafts exactly like a model whose
+    configuration says B' (the synthetic weights do not depend on B), and B'
+    outside [1, B] is refused."""
+    m, cfg = _model("tiny_f32", block_size=7)
+    st = spec.prefill(m, synth.prompts(cfg)[0])
+    small = om.Model(cfg.with_(block_size=3))
+    np.testing.assert_array_equal(spec.at_block_size(m, 3).draft_forward(st.anchor, st.dcache),
+                                  small.draft_forward(st.anchor, st.dcache))
+    for bad in (0, 8):
+        with pytest.raises(ValueError):
+            spec.at_block_size(m, bad)
+
+
 # ------------------------------------------------------------- cache pins
 def _committed_tokens(st):
     seq = np.concatenate([st.prompt, np.array(st.generated, dtype=np.int64)])
     return seq[: st.committed]
 
 
-def test_incremental_context_equals_recompute():
+@pytest.mark.parametrize("schedule", [None, [4, 2, 1, 3]])
+def test_incremental_context_equals_recompute(schedule):
     """Context K/V built round by round from verify passes (a+1 rows each)
     equals the context K/V recomputed from a fresh target pass over the
-    committed sequence."""
+    committed sequence (also when the block size changes between rounds)."""
     m, cfg = _model("tiny_f32_b3")
     p = synth.prompts(cfg)[1]
     ar, _ = spec.ar_generate(m, p, 30)
-    st = spec.generate(m, p, 30, proposer=spec.planted_proposer(ar, [3, 1, 4, 2], cfg.vocab))
+    st = spec.generate(m, p, 30, proposer=spec.planted_proposer(ar, [3, 1, 4, 2], cfg.vocab),
+                       block_schedule=schedule)
     seq = _committed_tokens(st)
     assert st.dcache.length == st.tcache.length == st.committed == len(p) + sum(r.accepted + 1 for r in st.rounds)
     tc, dc = m.new_target_cache(), m.new_draft_cache()
