@@ -19,6 +19,7 @@
 
 #include "dflash.h"
 #include "launch.h"
+#include "loss.h"
 
 using namespace dfl;
 

@@ -206,11 +206,6 @@ void verify_sample(const Launch& L, const float* logits, const float* dlogits, i
                    const float* temp, const int* proposal, const float* u_verify, float2* tstat, const float2* dstat,
                    int* n, int* anchor, int* accepted, int* bonus, int* ctx_row_seq, int* ctx_row_pos);
 
-// Training loss rows (sampling.cu): out[i*(B-1) + k-1] = -log softmax(logits of row
-// (first_seq + i)*B + k)[labels[i*(B-1) + k-1]] for i < n_seqs, k = 1 .. B-1.
-void row_nll(const Launch& L, const float* logits, int V, int B, int first_seq, int n_seqs, const int* labels,
-             float* out);
-
 // ---- round bookkeeping
 // Block rows of a draft (proposal == nullptr) or verify pass: token of row
 // s*B+j is anchor[s] (j == 0), the mask id (draft) or proposal[s*(B-1)+j-1]

@@ -14,6 +14,7 @@
 #include <math.h>
 
 #include "launch.h"
+#include "loss.h"
 
 namespace dfl {
 
