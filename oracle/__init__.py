@@ -23,7 +23,9 @@ Pins (checked by ``tests/test_oracle_*.py`` against the pages and the
 mathematics, not against this code):
 
 * speculative greedy output == plain AR greedy output (losslessness),
-  for several block sizes, batch shapes and proposers, including block 1;
+  for several block sizes, batch shapes and proposers, including block 1,
+  and with the block size changed between rounds (``spec.at_block_size``:
+  planted proposals accept exactly min(tau, B') - 1 drafts);
 * the drafter's incremental context cache == a from-scratch recomputation of
   every context feature and key/value from the committed sequence;
 * the verify pass with cache rollback == a fresh causal forward of the
