@@ -359,6 +359,10 @@ def run_ours(args, rank, world, local):
     max_seq = max(w.prompt_lens) + rounds * B + 4 * B
     t0 = time.time()
     sess = Session(w, max_seq_len=max_seq)
+    if args.runtime_block:
+        # rounds at a smaller block than the drafter's configured one (same weights and caches)
+        sess.set_block_size(args.runtime_block)
+        B = args.runtime_block
     t_init = time.time() - t0
     prompts = synth.prompts(w)
     t0 = time.time()
@@ -473,7 +477,7 @@ def run_ours(args, rank, world, local):
         "ms_per_step": h["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic (seeded random-init weights N(0,0.02), uniform prompt ids)",
         "config": {"workload": w.name, "batch": b, "prompt_len": list(w.prompt_lens)[:4], "block": B,
-                   "tau": 6.5, "draft_layers": w.draft_layers, "target_layers": w.target_layers,
+                   "configured_block": w.block_size, "tau": 6.5, "draft_layers": w.draft_layers, "target_layers": w.target_layers,
                    "l2": "inputs larger than L2: every round streams all weights (~19.7 GB)",
                    "parallelism": f"replicas x{world}"},
         "t_draft_ms": h["t_draft_ms"], "t_verify_ms": h["t_verify_ms"], "tau": h["tau"],
@@ -600,6 +604,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--block", type=int, default=0, help="block size B (default: the workload's, 16)")
+    ap.add_argument("--runtime-block", type=int, default=0, metavar="B",
+                    help="run the rounds at block B below the configured one (dflash_set_block_size)")
     ap.add_argument("--temperature", type=float, default=0.0,
                     help="T > 0: time sampled rounds (speculative rejection sampling) instead of greedy ones")
     ap.add_argument("--train-forward", type=int, default=0, metavar="M",
