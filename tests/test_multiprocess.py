@@ -32,7 +32,7 @@ def _rank_main(rank, world, port, tokens, seconds, out):
 @pytest.mark.parametrize("world", [2])
 def test_job_throughput_sums_tokens_over_the_slowest_rank(world):
     tokens, seconds = [100.0, 300.0], [1.0, 2.5]
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:   # no fork of a multi-threaded process
         out = mgr.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), tokens, seconds, out), nprocs=world, join=True)
         res = dict(out)
