@@ -128,7 +128,8 @@ def job_throughput(tokens_local: float, seconds_local: float, world: int):
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
-        d = json.load(open(p))
+        with open(p) as f:
+            d = json.load(f)
         return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
     return 6800.0, 1900.0, 1700.0, "fallback"
 
@@ -138,7 +139,8 @@ def kernel_source_hash(files=None) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_diffusion_speculative_ctx_gb300", "csrc")
     for f in sorted(files if files else os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -148,7 +150,8 @@ def ncu_traffic(kernel_class: str, workload: str):
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
+    with open(p) as f:
+        d = json.load(f)
     e = d.get(workload, {}).get(kernel_class)
     if not e or e.get("source_hash") != kernel_source_hash(e.get("sources")):
         return None

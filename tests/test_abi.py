@@ -23,7 +23,8 @@ def lib():
 def declared_functions():
     names = set()
     for h in HEADERS:
-        src = open(h).read()
+        with open(h) as f:
+            src = f.read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(dflash_\w+)\s*\(", src, flags=re.M):
             names.add(m.group(1))

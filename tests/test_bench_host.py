@@ -75,7 +75,8 @@ def test_peaks_fall_back_without_the_measured_file(tmp_path, monkeypatch):
 
 
 def test_committed_traffic_record_names_existing_sources():
-    d = json.load(open(os.path.join(os.path.dirname(bench.__file__), "profiles", "traffic.json")))
+    with open(os.path.join(os.path.dirname(bench.__file__), "profiles", "traffic.json")) as f:
+        d = json.load(f)
     csrc = os.path.join(os.path.dirname(bench.__file__), "block_diffusion_speculative_ctx_gb300", "csrc")
     for wl in d.values():
         for e in wl.values():

@@ -17,7 +17,8 @@ import synth
 from synth import configs
 from oracle import model as om, sampling as sp, spec
 
-GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_values.json")))
+with open(os.path.join(os.path.dirname(__file__), "golden", "pages_values.json")) as _f:
+    GOLD = json.load(_f)
 
 
 def _grid(n):

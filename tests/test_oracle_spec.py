@@ -18,7 +18,8 @@ import synth
 from synth import configs
 from oracle import metrics, model as om, spec
 
-GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_values.json")))
+with open(os.path.join(os.path.dirname(__file__), "golden", "pages_values.json")) as _f:
+    GOLD = json.load(_f)
 
 
 def _model(name, **kw):

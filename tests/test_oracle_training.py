@@ -17,7 +17,8 @@ import synth
 from synth import configs
 from oracle import model as om, spec, training as tr
 
-GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_values.json")))
+with open(os.path.join(os.path.dirname(__file__), "golden", "pages_values.json")) as _f:
+    GOLD = json.load(_f)
 
 
 def _setup(name="tiny_f32"):
