@@ -10,6 +10,7 @@
  *   [review] "DFlash: Why a Diffusion Drafter Can Accelerate an Autoregressive
  *            Model" (technical review: §2.3 eq. 2, §4.1, Algorithm 1,
  *            §5.1 eq. 9-10).
+ * and, for the runtime block size only, the "DFlash" wiki page (Ablations).
  *
  * Conventions
  * -----------
