@@ -103,3 +103,20 @@ def test_anchor_range_is_checked():
         tr.training_loss(m, x, [0], 3.0)
     with pytest.raises(ValueError):
         tr.training_loss(m, x, [len(x) - w.block_size + 1], 3.0)
+
+
+@pytest.mark.parametrize("B,lam", [(16, 7.0), (10, 5.0), (4, 3.0)])
+def test_each_position_predicts_the_token_k_after_the_anchor_with_weight_k(B, lam):
+    """Closed form of eq. 12 for hand-made logits: every predicted row k = 1..B-1
+    puts (practically) all mass on x[a+k] except row k0, which is uniform over V;
+    the block loss is then exp(-(k0-1)/lambda) * log V.  A label shifted by one
+    position or a weight exponent off by one gives a different value."""
+    V, a = 40, 5
+    x = np.random.default_rng(7).integers(0, V, size=a + B + 3)
+    for k0 in range(1, B):
+        lg = np.full((B, V), -1e4)
+        for k in range(1, B):
+            lg[k, x[a + k]] = 0.0
+        lg[k0] = 0.0
+        want = np.exp(-(k0 - 1) / lam) * np.log(V)
+        assert abs(tr.block_loss(lg, x, a, lam) - want) < 1e-9 * want
