@@ -155,3 +155,29 @@ def test_round_pin_catches_resampling_from_the_target(monkeypatch):
     monkeypatch.setattr(sp, "residual", lambda p, q: (np.asarray(p, np.float64), 1.0))
     with pytest.raises(AssertionError):
         test_round_emits_its_first_token_with_the_target_law()
+
+
+def test_all_accepted_emits_the_bonus_from_the_last_block_row():
+    """Algorithm 1's last step: when every proposal survives (acceptance uniforms of 0
+    accept any token the target gives positive mass), the emitted token is the draw
+    from the target's law at the last block row, p_{B-1} -- the law after the last
+    proposal, not after the anchor or an earlier proposal."""
+    w = configs.get("tiny_f32").with_(name="toy_bonus", vocab=16, d_model=32, n_heads=2, n_kv_heads=1,
+                                      head_dim=16, ffn=64, target_layers=2, draft_layers=1, ctx_layer_ids=(0, 1),
+                                      block_size=4, prompt_lens=(6,), weight_std=0.5)
+    m = om.Model(w)
+    T, B1 = 0.7, w.block_size - 1
+    st0 = spec.prefill(m, synth.prompts(w)[0])
+    rng = np.random.default_rng(5)
+    seen_rows = set()
+    for u_emit in _grid(40):
+        st = copy.deepcopy(st0)
+        y, q, _ = sp.draft_sampled(m, st, T, rng.random(B1))
+        lg, _ = m.target_forward(np.concatenate([[st0.anchor], y]), st0.tcache.copy())
+        rd = sp.verify_sampled(m, st, y, q, T, np.zeros(B1), float(u_emit))
+        assert rd.accepted == B1
+        laws = [sp.softmax_t(lg[j], T) for j in range(w.block_size)]
+        draws = [sp.sample_inverse_cdf(pj, float(u_emit)) for pj in laws]
+        assert rd.bonus == draws[B1]
+        seen_rows.update(j for j in range(B1) if draws[j] != draws[B1])
+    assert seen_rows == set(range(B1))   # every other row's law would have given a different token somewhere
