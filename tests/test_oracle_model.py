@@ -1,0 +1,63 @@
+"""Pins of the oracle's context feature ("DFlash: Why a Diffusion Drafter Can
+Accelerate an Autoregressive Model" §5.1 eq. 9; "DFlash: Block Diffusion for
+Flash Speculative Decoding", Paper vs code "Feature indexing"): the fused
+feature is RMSNorm(W_c [h_l1; ...; h_lk]) of the residual stream after each
+selected target layer.  Each pin fails for a plausible slip: a dropped norm, a
+dropped layer block, or a hidden state taken one layer early."""
+import numpy as np
+import pytest
+
+import synth
+from synth import configs
+from oracle import model as om
+
+
+def _sel(name):
+    w = configs.get(name)
+    m = om.Model(w)
+    x = np.asarray(synth.prompts(w)[0], dtype=np.int64)
+    _, sel = m.target_forward(x, m.new_target_cache(), want_logits=False)
+    return w, m, x, sel
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "tiny_f32_b3"])
+def test_feature_rows_are_rms_normalised(name):
+    """Divided by its norm scale, every feature row has unit root-mean-square, and the
+    feature does not change when the selected states are scaled (RMSNorm after W_c)."""
+    w, m, x, sel = _sel(name)
+    f = m.fuse(sel)
+    g = f / m.w("fc_norm")
+    # eps (1e-6) keeps the RMS just below one: sqrt(ms / (ms + eps)) with ms ~ 3e-3 here;
+    # without the norm the rows would keep the raw scale of W_c h (RMS ~ 0.07)
+    rms = np.sqrt((g ** 2).mean(axis=-1))
+    assert np.all(rms <= 1.0) and np.all(rms > 0.99), rms
+    np.testing.assert_allclose(m.fuse(3.0 * sel), f, rtol=1e-2, atol=1e-3)
+
+
+def test_feature_uses_every_selected_layer():
+    w, m, x, sel = _sel("tiny_f32")
+    d, k = w.d_model, len(w.ctx_layer_ids)
+    f = m.fuse(sel)
+    for i in range(k):
+        s2 = sel.copy()
+        s2[:, i * d:(i + 1) * d] *= -1.0
+        assert np.abs(m.fuse(s2) - f).max() > 1e-3, f"layer block {i} does not reach the feature"
+
+
+@pytest.mark.parametrize("layer", [0, 1, 3])
+def test_selected_state_is_the_residual_after_the_layer(layer):
+    """A model cut after target layer l (same weights) feeds its final norm exactly the
+    state the full model selects for layer l: the residual after layer l (0-based)."""
+    w = configs.get("tiny_f32").with_(ctx_layer_ids=(0, 1, 3))
+    m = om.Model(w)
+    x = np.asarray(synth.prompts(w)[0], dtype=np.int64)
+    _, sel = m.target_forward(x, m.new_target_cache(), want_logits=False)
+    i = w.ctx_layer_ids.index(layer)
+    h = sel[:, i * w.d_model:(i + 1) * w.d_model]
+    cut = om.Model(w.with_(target_layers=layer + 1, ctx_layer_ids=(layer,)), weights=m.w)
+    lg_cut, _ = cut.target_forward(x, cut.new_target_cache())
+    np.testing.assert_allclose(m.logits(h, "final_norm"), lg_cut, rtol=1e-9, atol=1e-9)
+    if layer > 0:   # the state one layer earlier is a different one
+        prev = om.Model(w.with_(target_layers=layer, ctx_layer_ids=(layer - 1,)), weights=m.w)
+        lg_prev, _ = prev.target_forward(x, prev.new_target_cache())
+        assert np.abs(m.logits(h, "final_norm") - lg_prev).max() > 1e-3
