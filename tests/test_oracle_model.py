@@ -61,3 +61,19 @@ def test_selected_state_is_the_residual_after_the_layer(layer):
         prev = om.Model(w.with_(target_layers=layer, ctx_layer_ids=(layer - 1,)), weights=m.w)
         lg_prev, _ = prev.target_forward(x, prev.new_target_cache())
         assert np.abs(m.logits(h, "final_norm") - lg_prev).max() > 1e-3
+
+
+def test_context_values_are_linear_in_the_feature():
+    """Context injection (eq. 10): V = W_V f with no norm in between, so doubling the
+    feature doubles the stored values; K = RoPE(k_norm(W_K f)) is per-head normalised,
+    so it does not change.  An extra RMSNorm of the feature before the projections
+    would make V scale-invariant, and a missing k-norm would double K."""
+    w, m, x, sel = _sel("tiny_f32_b3")
+    f = m.fuse(sel)
+    c1, c2 = m.new_draft_cache(), m.new_draft_cache()
+    m.append_context(f, c1)
+    m.append_context(2.0 * f, c2)
+    for l in range(w.draft_layers):
+        np.testing.assert_allclose(c2.v[l], 2.0 * c1.v[l], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(c2.k[l], c1.k[l], rtol=1e-3, atol=1e-4)
+        assert np.abs(c1.k[l]).max() > 1e-2
