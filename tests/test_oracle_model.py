@@ -77,3 +77,30 @@ def test_context_values_are_linear_in_the_feature():
         np.testing.assert_allclose(c2.v[l], 2.0 * c1.v[l], rtol=1e-12, atol=1e-15)
         np.testing.assert_allclose(c2.k[l], c1.k[l], rtol=1e-3, atol=1e-4)
         assert np.abs(c1.k[l]).max() > 1e-2
+
+
+def _layer_model(d, gate_scale):
+    """A model whose layer t0 has W_o = I, unit norms, W_gate = s I, W_up = I, W_down = I."""
+    w = configs.get("tiny_f32").with_(d_model=d, ffn=d, n_heads=1, n_kv_heads=1, head_dim=d)
+    eye = np.eye(d)
+    mats = {"t0.wo": eye, "t0.mlp_norm": np.ones(d), "t0.w_gate": gate_scale * eye, "t0.w_up": eye,
+            "t0.w_down": eye}
+    return w, om.Model(w, weights=om.Weights(lambda name: mats[name]), act_round=False)
+
+
+def test_swiglu_gates_through_silu_of_the_gate_projection():
+    """x + W_down (silu(W_gate xn) * W_up xn) with xn = rms_norm(x): with W_gate = g I for a
+    large |g|, silu(g z) tends to max(g z, 0), so the update is max(g xn, 0) * xn -- open where
+    g xn > 0, closed elsewhere.  Applying the SiLU to the up projection instead, or swapping
+    the two projections, gives another update."""
+    d, s = 64, 60.0
+    x = np.random.default_rng(2).normal(size=(3, d))
+    att = np.zeros((3, 1, d))                   # no attention update: only the MLP acts
+    for g in (s, -s):
+        w, m = _layer_model(d, g)
+        xn = om.rms_norm(x, np.ones(d), w.rms_eps)
+        want = x + np.maximum(g * xn, 0.0) * xn
+        big = np.abs(xn) > 0.2                  # away from the kink: silu(g z) = max(g z, 0) to ~1e-4
+        got = m._attn_out_mlp("t0", x, att)
+        np.testing.assert_allclose(got[big], want[big], rtol=1e-4, atol=1e-4)
+        assert np.abs(got - x)[big].max() > 1.0  # the MLP really acts
