@@ -104,3 +104,25 @@ def test_swiglu_gates_through_silu_of_the_gate_projection():
         got = m._attn_out_mlp("t0", x, att)
         np.testing.assert_allclose(got[big], want[big], rtol=1e-4, atol=1e-4)
         assert np.abs(got - x)[big].max() > 1.0  # the MLP really acts
+
+
+def test_one_token_layer_is_pre_norm_with_residuals():
+    """A one-token pass through a layer with W_v = W_o = I and a closed MLP gate (W_gate = 0,
+    silu(0) = 0): the token attends only to itself, so the residual after the layer is
+    e + rms_norm(e) (pre-norm attention input, values of the normalised input, residual
+    add), and the logits through an identity head are rms_norm(e + rms_norm(e))."""
+    d = 32
+    w = configs.get("tiny_f32").with_(d_model=d, ffn=d, n_heads=2, n_kv_heads=2, head_dim=d // 2, vocab=d,
+                                      target_layers=1, ctx_layer_ids=(0,), target_qk_norm=False)
+    rng = np.random.default_rng(9)
+    eye = np.eye(d)
+    mats = {"embed": rng.normal(size=(d, d)), "t0.attn_norm": np.ones(d), "t0.wq": rng.normal(size=(d, d)),
+            "t0.wk": rng.normal(size=(d, d)), "t0.wv": eye, "t0.wo": eye, "t0.mlp_norm": np.ones(d),
+            "t0.w_gate": np.zeros((d, d)), "t0.w_up": eye, "t0.w_down": eye, "final_norm": np.ones(d), "head": eye}
+    m = om.Model(w, weights=om.Weights(lambda name: mats[name]), act_round=False)
+    tok = 5
+    lg, sel = m.target_forward([tok], m.new_target_cache())
+    e = mats["embed"][tok]
+    after = e + om.rms_norm(e, np.ones(d), w.rms_eps)
+    np.testing.assert_allclose(sel[0], after, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lg[0], om.rms_norm(after, np.ones(d), w.rms_eps), rtol=1e-12, atol=1e-12)
