@@ -27,6 +27,9 @@
  * - Device-side checks (for example a token id outside [0, vocab) passed in
  *   device memory) never fault: they record an error word that the next
  *   synchronising call turns into DFLASH_E_DEVICE_CHECK.
+ * - One session serves one host thread at a time (calls on a ctx must not
+ *   overlap); separate sessions are independent and may be driven from
+ *   different threads.  dflash_init's error text is kept per thread.
  */
 #ifndef DFLASH_H
 #define DFLASH_H
