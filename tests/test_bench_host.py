@@ -82,3 +82,25 @@ def test_committed_traffic_record_names_existing_sources():
         for e in wl.values():
             assert all(os.path.exists(os.path.join(csrc, f)) for f in e["sources"])
             assert e["dram_bytes_per_launch"] > 0
+
+
+def test_oracle_baseline_is_one_sequence_at_a_time(monkeypatch):
+    """The CPU oracle handles a batch sequence by sequence: its tokens/s at planted tau is
+    tau over the time of one sequence's round, whatever the batch, and the line carries the
+    draft / verify split of the median sample."""
+    from synth import configs
+    times = iter([(0.5, 0.1, 0.4), (0.3, 0.1, 0.2), (0.4, 0.1, 0.3)])
+
+    def fake(w, ctx, state=None):
+        s, td, tv = next(times)
+        st = state or [None, None, None, None, [0.0, 0.0]]
+        st[4][0], st[4][1] = td, tv
+        return s, st
+
+    monkeypatch.setattr(bench, "cpu_sample_round_s", fake)
+    for batch in (1, 8):
+        times = iter([(0.5, 0.1, 0.4), (0.3, 0.1, 0.2), (0.4, 0.1, 0.3)] + [(0.4, 0.1, 0.3)] * 5)
+        b = bench.cpu_baseline(configs.get("qwen3_8b_b1_p512").with_(batch=batch), budget_s=0.0)
+        assert b["kind"] == "oracle" and abs(b["value"] - 6.5 / b["s_per_round"]) < 1e-12
+        assert b["s_per_round"] in (0.5, 0.4, 0.3)
+        assert abs(b["t_draft_ms"] + b["t_verify_ms"] - 1e3 * b["s_per_round"]) < 1e-9
