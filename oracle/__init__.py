@@ -44,11 +44,16 @@ mathematics, not against this code):
 * training: the packed block-sparse pass equals one pass per anchor, a block
   equals the inference draft pass with the same context and anchor token, no
   block sees a token at or after its anchor (or another block), the review's
-  lambda table and final weight, and the closed-form loss of a uniform drafter.
+  lambda table and final weight, and the closed-form loss of a uniform drafter;
+* the drafter's block pass, by hand-made drafters with closed-form outputs:
+  the drafts are the shared head's argmax on the B-1 mask rows (the anchor
+  row dropped, rows embedded with the target's table); the block's queries
+  are RMS-normalised per head (scaling W_q changes nothing); the block sits
+  at positions n .. n+B-1 right after the n context entries (each row picks
+  the context key whose RoPE angle matches its own position).
 
-Parity unpinned: the drafter's numerical output as a whole.  No trained draft
-weights exist here, so nothing outside this code fixes what a random-init
-drafter should propose beyond the structural pins above (context injection,
-bidirectional attention, cache reuse and immutability).
+What no pin can fix here is what a trained drafter proposes (its acceptance
+length): no trained weights exist, so only the structure and arithmetic of
+the drafter's pass are pinned, not its quality.
 """
 from . import metrics, model, sampling, spec, training  # noqa: F401

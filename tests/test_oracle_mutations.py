@@ -95,3 +95,74 @@ def test_attention_without_scale_is_caught():
     from tests.test_oracle_primitives import _attention_loops
     bad = om.attention(q * np.sqrt(8), k, v, vis)          # i.e. scores not divided by sqrt(hd)
     assert not np.allclose(bad, _attention_loops(q, k, v, vis))
+
+
+# ------------------------------------------------ the drafter's block pass
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except AssertionError:
+        return True
+    return False
+
+
+def test_draft_of_the_wrong_rows_is_caught(monkeypatch):
+    """Argmax over rows 0..B-2 (keeping the anchor row, dropping the last mask row)."""
+    from tests import test_oracle_drafter as pins
+
+    def bad_draft(model, st):
+        lg = model.draft_forward(st.anchor, st.dcache)
+        return om.argmax_lowest(lg[:-1]), lg
+
+    monkeypatch.setattr(spec, "draft", bad_draft)
+    assert _fails(pins.test_drafts_are_the_mask_rows_argmax_through_the_shared_head, 4)
+
+
+def test_missing_query_norm_in_the_drafter_is_caught(monkeypatch):
+    """Block queries without the per-head RMSNorm (keys still normalised)."""
+    from tests import test_oracle_drafter as pins
+    orig = om.Model._qkv
+
+    def qkv_without_qnorm(self, p, x, pos, qk_norm):
+        if not p.startswith("d"):
+            return orig(self, p, x, pos, qk_norm)
+        c, w = self.cfg, self.w
+        n = x.shape[0]
+        xn = self.r(om.rms_norm(x, w(f"{p}.attn_norm"), c.rms_eps))
+        q = (xn @ w(f"{p}.wq").T).reshape(n, c.n_heads, c.head_dim)
+        k = (xn @ w(f"{p}.wk").T).reshape(n, c.n_kv_heads, c.head_dim)
+        v = (xn @ w(f"{p}.wv").T).reshape(n, c.n_kv_heads, c.head_dim)
+        k = om.rms_norm(k, w(f"{p}.k_norm"), c.rms_eps)
+        return (self.r(om.rope(q, pos, c.rope_theta)), self.r(om.rope(k, pos, c.rope_theta)), self.r(v))
+
+    monkeypatch.setattr(om.Model, "_qkv", qkv_without_qnorm)
+    assert _fails(pins.test_block_queries_are_rms_normalised, "tiny_f32")
+    assert _fails(pins.test_block_queries_are_rms_normalised, "tiny_f32_b3")
+
+
+def _draft_forward_at(shift_fn):
+    """The oracle's draft pass with block positions shift_fn(n0, B) instead of n0 .. n0+B-1."""
+    def draft_forward(self, anchor, cache):
+        c, w = self.cfg, self.w
+        B, n0 = c.block_size, cache.length
+        pos = shift_fn(n0, B)
+        tokens = np.array([anchor] + [c.mask_token] * (B - 1), dtype=np.int64)
+        h = w("embed")[tokens].copy()
+        for l in range(c.draft_layers):
+            p = f"d{l}"
+            q, kb, vb = self._qkv(p, h, pos, True)
+            K = np.concatenate([cache.k[l], kb], axis=0)
+            V = np.concatenate([cache.v[l], vb], axis=0)
+            att = om.attention(q, K, V, np.ones((B, n0 + B), dtype=bool))
+            h = self._attn_out_mlp(p, h, att)
+        return self.logits(h, "draft_norm")
+    return draft_forward
+
+
+@pytest.mark.parametrize("shift", [lambda n0, B: np.arange(n0 + 1, n0 + B + 1),   # one position late
+                                   lambda n0, B: np.arange(n0 - 1, n0 + B - 1),   # one position early
+                                   lambda n0, B: np.arange(0, B)])                # positions from 0
+def test_block_position_offset_is_caught(monkeypatch, shift):
+    from tests import test_oracle_drafter as pins
+    monkeypatch.setattr(om.Model, "draft_forward", _draft_forward_at(shift))
+    assert _fails(pins.test_block_sits_at_positions_n_to_n_plus_B_minus_1, 9)
