@@ -41,10 +41,10 @@ constexpr int GEMM_COUNTERS = 1 << 16;
 enum State { ST_EMPTY = 0, ST_READY = 1, ST_DRAFTED = 2 };
 
 struct LayerW {
-    void* wqkv = nullptr;   // [(H + 2 Hkv) hd, d]: rows wq, wk, wv
-    void* wo = nullptr;     // [d, H hd]
-    void* wgu = nullptr;    // [2F, d]: rows w_gate, w_up
-    void* wdown = nullptr;  // [d, F]
+    void* wqkv = nullptr;         // [(H + 2 Hkv) hd, d]: rows wq, wk, wv (library-owned copy)
+    const void* wo = nullptr;     // [d, H hd] (the caller's buffer, borrowed)
+    void* wgu = nullptr;          // [2F, d]: rows w_gate, w_up (library-owned copy)
+    const void* wdown = nullptr;  // [d, F] (borrowed)
     float* attn_norm = nullptr;
     float* mlp_norm = nullptr;
     float* q_norm = nullptr;
@@ -67,9 +67,10 @@ struct dflash_ctx {
     int ctx_slot[64];  // target layer -> index in ctx_layer_ids or -1
 
     std::vector<LayerW> tl, dl;
-    void* embed = nullptr;
-    void* head = nullptr;
-    void* fc = nullptr;
+    // borrowed from the caller: used in place, never freed here
+    const void* embed = nullptr;
+    const void* head = nullptr;
+    const void* fc = nullptr;
     float* final_norm = nullptr;
     float* fc_norm = nullptr;
     float* draft_norm = nullptr;
@@ -287,18 +288,25 @@ dflash_status copy_norm(dflash_ctx* c, float** dst, const float* src, size_t n, 
     return DFLASH_OK;
 }
 
+// A weight used in place: non-NULL and 16-byte aligned (tensor-map and vector loads).
+dflash_status borrow(dflash_ctx* c, const void** dst, const void* src, const char* what) {
+    if (!src) return c->fail(DFLASH_E_INVAL, "weight %s is NULL", what);
+    if ((uintptr_t)src & 15u) return c->fail(DFLASH_E_INVAL, "weight %s is not 16-byte aligned", what);
+    *dst = src;
+    return DFLASH_OK;
+}
+
 dflash_status pack_layer(dflash_ctx* c, const dflash_layer_weights& w, LayerW& o, bool qk_norm) {
     const size_t d = c->d, F = c->F, qd = c->qd, kvd = c->kvd;
-    o.wqkv = dev_alloc(c, (qd + 2 * kvd) * d * c->esz);
-    o.wo = dev_alloc(c, d * qd * c->esz);
-    o.wgu = dev_alloc(c, 2 * F * d * c->esz);
-    o.wdown = dev_alloc(c, d * F * c->esz);
-    if (!o.wqkv || !o.wo || !o.wgu || !o.wdown) return c->fail(DFLASH_E_NOMEM, "weight allocation failed");
     dflash_status s;
+    if ((s = borrow(c, &o.wo, w.wo, "wo"))) return s;
+    if ((s = borrow(c, &o.wdown, w.w_down, "w_down"))) return s;
+    o.wqkv = dev_alloc(c, (qd + 2 * kvd) * d * c->esz);
+    o.wgu = dev_alloc(c, 2 * F * d * c->esz);
+    if (!o.wqkv || !o.wgu) return c->fail(DFLASH_E_NOMEM, "weight allocation failed");
     if ((s = copy_rows(c, o.wqkv, 0, w.wq, qd, d))) return s;
     if ((s = copy_rows(c, o.wqkv, qd, w.wk, kvd, d))) return s;
     if ((s = copy_rows(c, o.wqkv, qd + kvd, w.wv, kvd, d))) return s;
-    if ((s = copy_rows(c, o.wo, 0, w.wo, d, qd))) return s;
     if (c->cfg.dtype == DFLASH_DTYPE_BF16) {
         // SwiGLU epilogue layout: tile j = gate rows [64j, 64j+64) then up rows [64j, 64j+64)
         if (!w.w_gate || !w.w_up) return c->fail(DFLASH_E_INVAL, "a weight pointer is NULL");
@@ -310,7 +318,6 @@ dflash_status pack_layer(dflash_ctx* c, const dflash_layer_weights& w, LayerW& o
         if ((s = copy_rows(c, o.wgu, 0, w.w_gate, F, d))) return s;
         if ((s = copy_rows(c, o.wgu, F, w.w_up, F, d))) return s;
     }
-    if ((s = copy_rows(c, o.wdown, 0, w.w_down, d, F))) return s;
     if ((s = copy_norm(c, &o.attn_norm, w.attn_norm, d, false))) return s;
     if ((s = copy_norm(c, &o.mlp_norm, w.mlp_norm, d, false))) return s;
     if (qk_norm) {
@@ -974,14 +981,12 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     } while (0)
 
     const size_t d = c->d, V = c->V, esz = c->esz;
-    // weights
-    ALLOC(c->embed, V * d * esz);
-    ALLOC(c->head, V * d * esz);
-    ALLOC(c->fc, d * c->k * d * esz);
+    // weights: embedding, head, W_c, wo and w_down are used in place; wq/wk/wv and
+    // w_gate/w_up are packed into library-owned matrices
     dflash_status s;
-    if ((s = copy_rows(c, c->embed, 0, w->embed, V, d))) return bail(s);
-    if ((s = copy_rows(c, c->head, 0, w->head, V, d))) return bail(s);
-    if ((s = copy_rows(c, c->fc, 0, w->fc, d, c->k * d))) return bail(s);
+    if ((s = borrow(c, &c->embed, w->embed, "embed"))) return bail(s);
+    if ((s = borrow(c, &c->head, w->head, "head"))) return bail(s);
+    if ((s = borrow(c, &c->fc, w->fc, "fc"))) return bail(s);
     if ((s = copy_norm(c, &c->final_norm, w->final_norm, d, false))) return bail(s);
     if ((s = copy_norm(c, &c->fc_norm, w->fc_norm, d, false))) return bail(s);
     if ((s = copy_norm(c, &c->draft_norm, w->draft_norm, d, false))) return bail(s);

@@ -50,11 +50,24 @@ dflash_status fail(dflash_status s, const char* msg) {
     return s;
 }
 
+// out[r] = -1 for every row when a bounded device-side wait of this call ran out
+// (the error word is cleared at the start of each call).
+__global__ void poison_on_error_kernel(const uint32_t* __restrict__ err, int rows, int* __restrict__ out) {
+    if (*err == 0u) return;
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) out[r] = -1;
+}
+
+// Queues the norm, the head GEMM, the row argmax and the error check; false when a
+// kernel could not be prepared (for example a tensor map that could not be encoded).
 template <typename T>
-void run_head(const float* x, const float* norm_w, float eps, const void* head, int rows, int d, int vocab, int* out,
+bool run_head(const float* x, const float* norm_w, float eps, const void* head, int rows, int d, int vocab, int* out,
               unsigned char* scratch, cudaStream_t stream) {
+    bool failed = false;
     Launch L{stream, nullptr};
-    L.err = reinterpret_cast<uint32_t*>(scratch);  // first 256 bytes: device error word
+    L.failed = &failed;
+    uint32_t* err = reinterpret_cast<uint32_t*>(scratch);  // first 256 bytes: device error word
+    L.err = err;
+    if (cudaMemsetAsync(err, 0, sizeof(uint32_t), stream) != cudaSuccess) return false;
     scratch += 256;
     T* xn = reinterpret_cast<T*>(scratch);
     const size_t xn_bytes = ((size_t)rows * d * sizeof(T) + 255) / 256 * 256;
@@ -62,6 +75,8 @@ void run_head(const float* x, const float* norm_w, float eps, const void* head, 
     rmsnorm_rows<T>(L, x, d, norm_w, rows, d, eps, xn, d);
     gemm<T>(L, xn, d, reinterpret_cast<const T*>(head), rows, vocab, d, logits, vocab, false);
     argmax_rows(L, logits, vocab, rows, vocab, out);
+    launch_k(L, poison_on_error_kernel, dim3((rows + 255) / 256), dim3(256), 0, 1, (const uint32_t*)err, rows, out);
+    return !failed;
 }
 
 }  // namespace
@@ -73,6 +88,9 @@ extern "C" dflash_status dflash_head_argmax_noalloc(int32_t dtype, const float* 
     if (dtype != DFLASH_DTYPE_F32 && dtype != DFLASH_DTYPE_BF16) return fail(DFLASH_E_INVAL, "dtype must be F32 or BF16");
     if (rows < 1 || d_model < 8 || d_model % 8 || vocab < 1 || !(eps > 0.f))
         return fail(DFLASH_E_INVAL, "rows >= 1, d_model a positive multiple of 8, vocab >= 1 and eps > 0 required");
+    // the head is read through TMA (bf16) and both matrices with 16-byte vector loads
+    if (((uintptr_t)x | (uintptr_t)head | (uintptr_t)norm_w) & 15u)
+        return fail(DFLASH_E_INVAL, "x, norm_w and head must be 16-byte aligned");
     const size_t esz = dtype == DFLASH_DTYPE_BF16 ? 2 : 4;
     const size_t need = 256 + ((size_t)rows * d_model * esz + 255) / 256 * 256 + (size_t)rows * vocab * 4;
     if (need > NOALLOC_SCRATCH_BYTES) {
@@ -86,11 +104,12 @@ extern "C" dflash_status dflash_head_argmax_noalloc(int32_t dtype, const float* 
     cudaError_t e = scratch_address(&scratch);
     if (e != cudaSuccess) return fail(DFLASH_E_CUDA, cudaGetErrorString(e));
     cudaStream_t s = (cudaStream_t)cuda_stream;
-    if (dtype == DFLASH_DTYPE_BF16)
-        run_head<bf16>(x, norm_w, eps, head, rows, d_model, vocab, out, (unsigned char*)scratch, s);
-    else
-        run_head<float>(x, norm_w, eps, head, rows, d_model, vocab, out, (unsigned char*)scratch, s);
+    const bool queued =
+        dtype == DFLASH_DTYPE_BF16
+            ? run_head<bf16>(x, norm_w, eps, head, rows, d_model, vocab, out, (unsigned char*)scratch, s)
+            : run_head<float>(x, norm_w, eps, head, rows, d_model, vocab, out, (unsigned char*)scratch, s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(DFLASH_E_CUDA, cudaGetErrorString(e));
+    if (!queued) return fail(DFLASH_E_CUDA, "a kernel of the head could not be prepared (tensor map or launch setup)");
     return DFLASH_OK;
 }

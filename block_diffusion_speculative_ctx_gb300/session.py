@@ -122,8 +122,10 @@ class Session:
         ws, keep = weights_struct(w, tens)
         self.ctx = dflash_init(self.cfg, ws, self.stream.cuda_stream)
         del keep
-        if tensors is None:
-            del tens
+        # the library reads embed, head, fc, wo and w_down in place for the session's lifetime;
+        # the other matrices were packed into its own buffers and may go
+        packed = {"wq", "wk", "wv", "w_gate", "w_up"}
+        self._borrowed = {k: t for k, t in tens.items() if k.rsplit(".", 1)[-1] not in packed}
         self.batch = 0
 
     # -------------------------------------------------------------- the round
@@ -274,6 +276,7 @@ class Session:
         if getattr(self, "ctx", None):
             dflash_destroy(self.ctx)
             self.ctx = None
+        self._borrowed = None
 
     def __del__(self):
         try:

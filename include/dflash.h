@@ -121,8 +121,13 @@ typedef struct {
     void* alloc_user;
 } dflash_config;
 
-/* One decoder layer.  Device pointers; read only inside dflash_init (the
- * library copies them into its own layout), so they may be freed afterwards. */
+/* One decoder layer, device pointers.  wq, wk, wv, w_gate and w_up are read
+ * only inside dflash_init, which packs them into library-owned matrices (one
+ * [q; k; v] projection, and in bf16 gate and up interleaved in 64-row tiles
+ * for the fused SwiGLU), so they may be freed afterwards.  wo and w_down are
+ * borrowed: every call reads them in place, so they must stay allocated and
+ * unchanged until dflash_destroy, and be 16-byte aligned.  Norm scales are
+ * copied. */
 typedef struct {
     const void* wq;            /* [H*hd, d] */
     const void* wk;            /* [H_kv*hd, d] */
@@ -139,7 +144,8 @@ typedef struct {
 
 /* Target decoder plus drafter.  The drafter shares the target's embedding
  * table and LM head ([digest] Method, Training §4.2 step 6; Paper vs code
- * "Embedding and head"). */
+ * "Embedding and head").  embed, head and fc are borrowed like wo and w_down
+ * (in place until dflash_destroy, 16-byte aligned). */
 typedef struct {
     const void* embed;                     /* [V, d] */
     const void* head;                      /* [V, d] */
@@ -165,9 +171,14 @@ typedef struct dflash_ctx dflash_ctx; /* opaque; owned by the library */
 
 /* Create a session: validate cfg, allocate the paged target KV cache, the
  * draft context cache and all round buffers for max_batch x max_seq_len
- * (nothing is allocated later), and pack the weights into the library's
- * layout.  cuda_stream is a cudaStream_t (NULL = legacy default stream).
- * Errors: E_INVAL (cfg), E_NOMEM, E_CUDA.  *out is NULL on failure. */
+ * (nothing is allocated later), and pack the q/k/v and gate/up matrices into
+ * the library's layout.  Those packed copies are the session's only weight
+ * memory: (H + 2 H_kv) hd d + 2 F d elements per layer, about 13 of the 19.7 GB
+ * of a Qwen3-8B-shaped target with its 5-layer drafter; the caller's wq, wk, wv,
+ * w_gate and w_up may be freed once this returns, and every other matrix is
+ * used in place.  cuda_stream is a cudaStream_t (NULL = legacy default stream).
+ * Errors: E_INVAL (cfg, a NULL or misaligned borrowed weight), E_NOMEM, E_CUDA.
+ * *out is NULL on failure. */
 dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, void* cuda_stream,
                           dflash_ctx** out);
 
@@ -336,7 +347,12 @@ enum { DFLASH_NOALLOC_SCRATCH_BYTES = 16 << 20 };
  * library is loaded.  Such a caller cannot create a session (dflash_init
  * allocates), but can still pick tokens from final hidden states with this
  * call: out[r] = argmax_v ( RMSNorm(x[r]) * norm_w ) . head[v], ties to the
- * lowest id - the same kernels dflash_verify uses for its posterior.
+ * lowest id.  It queues three kernels - an RMSNorm of the rows into the
+ * element type of head, the head GEMM (tensor cores for bf16), and a row
+ * argmax - plus a check of its error word.  dflash_verify computes the same
+ * quantity with the norm and the argmax fused into its head GEMM; in bf16 the
+ * two can pick different tokens where the two largest logits lie within
+ * bf16 rounding of each other.
  *
  * Arguments (all device pointers except cuda_stream):
  *   dtype   DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16: element type of head
@@ -345,21 +361,28 @@ enum { DFLASH_NOALLOC_SCRATCH_BYTES = 16 << 20 };
  *   head    [vocab, d_model] LM head
  *   out     int32 [rows] token ids (written)
  *   cuda_stream  cudaStream_t the kernels are queued on (NULL = legacy default)
- * The call queues its kernels and returns without synchronising.
+ * x, norm_w and head must be 16-byte aligned.  The call queues its kernels and
+ * returns without synchronising.
  *
  * Memory: it allocates nothing.  Its intermediates (the normalised rows and
  * the fp32 logits, rows * (d_model * elem + vocab * 4) bytes plus alignment)
- * live in one fixed array of DFLASH_NOALLOC_SCRATCH_BYTES (16 MiB) that every
- * GPU which loads this library holds until the process exits.  Larger
- * requests are rejected with DFLASH_E_INVAL before anything is queued (for
- * example at vocab 151936 and d_model 4096 in bf16, up to 27 rows fit).
+ * and a device error word live in one fixed array of
+ * DFLASH_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads this
+ * library holds until the process exits.  Larger requests are rejected with
+ * DFLASH_E_INVAL before anything is queued (for example at vocab 151936 and
+ * d_model 4096 in bf16, up to 27 rows fit).
  * The first call on each device looks up that array's device address with
  * the device current; make that first call before any CUDA stream capture.
- * All calls share the array and it keeps the last call's contents; no part of
- * it needs to start at zero.  Calls that overlap on the GPU (on different
- * streams, or from different threads) race on the array: order them.
- * Errors: E_INVAL (NULL pointer, bad sizes, request above the maximum),
- * E_CUDA; the text is available from dflash_last_error(NULL). */
+ * All calls share the array and it keeps the last call's contents; each call
+ * clears its error word first, and nothing else needs to start at zero.
+ * Calls that overlap on the GPU (on different streams, or from different
+ * threads) race on the array: order them.
+ * Errors: E_INVAL (NULL or misaligned pointer, bad sizes, request above the
+ * maximum), E_CUDA (a launch failed or a kernel could not be prepared); the
+ * text is available from dflash_last_error(NULL).  Because the call does not
+ * synchronise, a failure on the device is reported in the output instead: if
+ * a bounded device-side wait inside the head GEMM ran out (it should never),
+ * every out[r] is -1, which is not a token id. */
 dflash_status dflash_head_argmax_noalloc(int32_t dtype, const float* x, const float* norm_w, float eps,
                                          const void* head, int32_t rows, int32_t d_model, int32_t vocab,
                                          int32_t* out, void* cuda_stream);
