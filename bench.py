@@ -22,6 +22,9 @@ Reported (one JSON line on rank 0):
   roofline     the dominant kernel class (CUDA-event profile of the round)
                against the measured HBM copy bandwidth
   cpu_baseline the CPU oracle on a bounded sample, extrapolated per round
+  secondary    (default workload only) the concurrency-32 ragged workload at tau = 6.5:
+               t_draft, t_verify, tokens/s, and its layer + head GEMMs' flops over
+               their time against the sustained bf16 tensor peak
 
 --impl reference times the CPU oracle alone on the same workload.
 """
@@ -69,7 +72,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -368,6 +371,10 @@ def run_ours(args, rank, world, local):
         B = args.runtime_block
     t_init = time.time() - t0
     prompts = synth.prompts(w)
+    # clocks are sampled from the start of the stream discovery (the GPU is busy from here on)
+    # to the end of the last timed region: the three tau regions and the e2e region lie inside
+    sampler = ClockSampler(local)
+    sampler.__enter__()
     t0 = time.time()
     streams = stream_for(sess, prompts, need, B)
     t_stream = time.time() - t0
@@ -391,15 +398,9 @@ def run_ours(args, rank, world, local):
         barrier()
         torch.cuda.synchronize()
         headline = tau_name == "6.5"
-        sampler = ClockSampler(local) if headline else None
-        if sampler:
-            sampler.__enter__()
         per, total_ms = timed_rounds(sess, props_dev, acc_dev, bon_dev, drafts_dev, W, K)
         torch.cuda.synchronize()
         barrier()
-        if sampler:
-            sampler.__exit__()
-            clocks = sampler.summary()
         launches = sess.stats().kernel_launches - l0
         got = acc_dev.cpu().numpy()[W:]
         tau = float(np.mean(got + 1))
@@ -435,7 +436,11 @@ def run_ours(args, rank, world, local):
         sess.draft_block(drafts_h)
         sess.verify(host_props[r], acc_h, bon_h)
         emitted += int(acc_h.sum()) + b
-    e2e_tps, e2e_s = job_throughput(float(emitted), time.perf_counter() - t0, world)
+    e2e_s_local = time.perf_counter() - t0
+    sampler.__exit__()
+    clocks = sampler.summary()
+    clocks["window"] = "stream discovery through the last timed region (tau 1, 4, 6.5 and e2e)"
+    e2e_tps, e2e_s = job_throughput(float(emitted), e2e_s_local, world)
     e2e = {"value": e2e_tps, "unit": "tokens/s",
            "h2d_bytes_per_step": int(b * max(B - 1, 0) * 4),
            "d2h_bytes_per_step": int(b * max(B - 1, 0) * 4 + 2 * b * 4),
@@ -492,10 +497,83 @@ def run_ours(args, rank, world, local):
         "prefill": {"ms": prefill_ms, "tokens": int(sum(w.prompt_lens)),
                     "tokens_per_s": sum(w.prompt_lens) / (prefill_ms * 1e-3) if prefill_ms > 0 else None},
     }
+    if world == 1 and not args.no_secondary and args.workload == DEFAULT_WORKLOAD and not args.block \
+            and not args.runtime_block:
+        line["secondary"] = run_secondary(SECONDARY_WORKLOAD, min(K, 20), W)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+SECONDARY_WORKLOAD = "qwen3_8b_c32_ragged"
+GEMM_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "gemm_fc", "gemm_ctx_kv")
+
+
+def run_secondary(name: str, K: int, W: int):
+    """The concurrency-32 workload at tau = 6.5, measured the same way as the headline
+    (planted proposals, K timed rounds after W warm-up rounds, CUDA events on the session
+    stream), plus a kernel-class profile pass whose GEMM flops over GEMM time are set
+    against the sustained bf16 peak (these GEMMs are compute-bound at 512 rows)."""
+    import numpy as np
+    import torch
+
+    import synth
+    from synth import configs
+    from block_diffusion_speculative_ctx_gb300 import Session
+
+    w = configs.get(name)
+    B, b = w.block_size, w.batch
+    rounds = W + K
+    need = rounds * 7 + B + 2
+    t0 = time.time()
+    sess = Session(w, max_seq_len=max(w.prompt_lens) + rounds * B + 4 * B)
+    prompts = synth.prompts(w)
+    streams = stream_for(sess, prompts, need, B)
+    props, accs = plan_proposals(streams, TAU_PLANS["6.5"], rounds, B, w.vocab)
+    props_dev = torch.from_numpy(props).cuda()
+    acc_dev = torch.zeros((rounds, b), dtype=torch.int32, device="cuda")
+    bon_dev = torch.zeros((rounds, b), dtype=torch.int32, device="cuda")
+    drafts_dev = torch.zeros((b, max(B - 1, 1)), dtype=torch.int32, device="cuda")
+    sess.prefill(prompts)
+    timed_rounds(sess, props_dev, acc_dev, bon_dev, drafts_dev, 0, W)
+    torch.cuda.synchronize()
+    per, total_ms = timed_rounds(sess, props_dev, acc_dev, bon_dev, drafts_dev, W, K)
+    got = acc_dev.cpu().numpy()[W:]
+    tokens = float((got + 1).sum())
+    td = statistics.median(p[0] for p in per)
+    tv = statistics.median(p[1] for p in per)
+    # kernel-class profile of the same rounds (events between launches: not the headline timing)
+    sess.prefill(prompts)
+    timed_rounds(sess, props_dev, acc_dev, bon_dev, drafts_dev, 0, W)
+    sess.profile_reset()
+    sess.set_profiling(True)
+    timed_rounds(sess, props_dev, acc_dev, bon_dev, drafts_dev, W, K)
+    sess.set_profiling(False)
+    prof = sess.profile()
+    p0 = sess.stats().prefill_ms
+    sess.prefill(prompts)
+    prefill_ms = sess.stats().prefill_ms - p0
+    sess.close()
+    _, _, tf_sus, peak_src = measured_peaks()
+    g_ms = sum(prof[k]["ms"] for k in GEMM_CLASSES if k in prof)
+    g_fl = sum(prof[k]["flops"] for k in GEMM_CLASSES if k in prof)
+    achieved = g_fl / (g_ms * 1e-3) / 1e12 if g_ms > 0 else 0.0
+    per_class = {k: {"ms_per_round": prof[k]["ms"] / K,
+                     "TFLOPs": prof[k]["flops"] / (prof[k]["ms"] * 1e-3) / 1e12 if prof[k]["ms"] > 0 else 0.0}
+                 for k in GEMM_CLASSES if k in prof and prof[k]["launches"]}
+    return {
+        "workload": w.name, "batch": b, "block": B, "tau": float(np.mean(got + 1)), "steps": K, "warmup": W,
+        "t_draft_ms": td, "t_verify_ms": tv, "ms_per_step": total_ms / K,
+        "tokens_per_s": tokens / (total_ms * 1e-3),
+        "roofline": {"kernel": "layer and head GEMMs of the round (all classes)", "bound": "tensor",
+                     "achieved": achieved, "peak": tf_sus, "unit": "TFLOP/s", "frac": achieved / tf_sus,
+                     "peak_source": peak_src + " (sustained bf16)", "gemm_ms_per_round": g_ms / K,
+                     "gemm_tflop_per_round": g_fl / K / 1e12, "traffic": None},
+        "gemms": per_class,
+        "prefill": {"ms": prefill_ms, "tokens": int(sum(w.prompt_lens))},
+        "setup_s": time.time() - t0,
+    }
 
 
 # --------------------------------------------------------- CPU oracle arm
@@ -582,25 +660,33 @@ def run_reference(args, rank, world):
     except Exception:
         cores = os.cpu_count() or 1
     _, st = cpu_sample_round_s(w, ctx)
+    n_warm = 0
     for _ in range(args.warmup):
         cpu_sample_round_s(w, ctx, st)
+        n_warm += 1
         if time.time() - args._t0 > 60:
             break
     per = []
     t0 = time.time()
     for i in range(args.steps):
+        t1 = time.perf_counter()
         s, _ = cpu_sample_round_s(w, ctx, st)
-        per.append((s, st[4][0], st[4][1]))
+        per.append((s, st[4][0], st[4][1], time.perf_counter() - t1))
         if time.time() - t0 > 150:                       # keep the whole run within a few minutes
             break
-    per_round, td, tv = sorted(per)[(len(per) - 1) // 2]   # the median sample (lower middle)
+    per_round, td, tv, wall = sorted(per)[(len(per) - 1) // 2]   # the median sample (lower middle)
     tau = 6.5
     value = oracle_tokens_per_s(tau, per_round)
+    # a step is one timed sample (one target layer + one draft layer + the head, at full width);
+    # ms_per_step is its measured wall time, and the full round is extrapolated from it
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": len(per), "warmup": args.warmup, "ms_per_step": per_round * 1e3, "higher_is_better": True,
+        "steps": len(per), "warmup": n_warm, "ms_per_step": wall * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "block": w.block_size, "tau": tau},
+        "step": "one sample: 1 target layer + 1 draft layer + the shared head over one block, fp64 oracle",
+        "extrapolated_round_ms": per_round * 1e3, "layers_sampled": {"target": 1, "draft": 1},
+        "layers_extrapolated": {"target": w.target_layers, "draft": w.draft_layers},
         "t_draft_ms": 1e3 * td, "t_verify_ms": 1e3 * tv,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": "fp64 numpy oracle, 1 target + 1 draft layer + head per step, scaled to the "
@@ -625,6 +711,8 @@ def main():
     ap.add_argument("--train-forward", type=int, default=0, metavar="M",
                     help="time the drafter's training forward with M anchor blocks instead of rounds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the concurrency-32 line that the default run adds (secondary)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ncu-target", action="store_true",
                     help="short fixed run for profiler launch lists (prints no benchmark line)")
