@@ -243,8 +243,14 @@ def run_ncu_target(args, local):
     dbuild.build()
     w = workload_of(args)
     B, b = w.block_size, w.batch
+    prompts = synth.prompts(w)
+    if args.ncu_prompt_len:
+        # shorter prompts: the prefill's GEMMs stay at or under 256 rows (the per-tile kernel),
+        # so a kernel filter on the persistent GEMM counts the round's launches only
+        prompts = [p[: args.ncu_prompt_len] for p in prompts]
+        w = w.with_(prompt_lens=tuple(len(p) for p in prompts))
     sess = Session(w, max_seq_len=max(w.prompt_lens) + (args.warmup + args.steps + 4) * B)
-    sess.prefill(synth.prompts(w))
+    sess.prefill(prompts)
     drafts = torch.zeros((b, max(B - 1, 1)), dtype=torch.int32, device="cuda")
     acc = torch.zeros((b,), dtype=torch.int32, device="cuda")
     bon = torch.zeros((b,), dtype=torch.int32, device="cuda")
@@ -716,6 +722,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ncu-target", action="store_true",
                     help="short fixed run for profiler launch lists (prints no benchmark line)")
+    ap.add_argument("--ncu-prompt-len", type=int, default=0, metavar="N",
+                    help="with --ncu-target: cut every prompt to its first N tokens")
     args = ap.parse_args()
     args._t0 = time.time()
     if args.warmup < 3:

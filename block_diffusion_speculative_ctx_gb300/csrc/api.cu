@@ -35,7 +35,7 @@ constexpr int PAGE_TOKENS = 64;
 constexpr int PAGE_SHIFT = 6;
 constexpr int PREFILL_CHUNK = 2048;
 constexpr size_t ATTN_WS_BYTES = 64ull << 20;
-constexpr size_t GEMM_WS_BYTES = 64ull << 20;
+constexpr size_t GEMM_WS_BYTES = 96ull << 20;  // stream-K partial tiles, one workspace per stream
 constexpr int GEMM_COUNTERS = 1 << 16;
 
 enum State { ST_EMPTY = 0, ST_READY = 1, ST_DRAFTED = 2 };
@@ -127,6 +127,8 @@ struct dflash_ctx {
     float* attn_ws = nullptr;
     float* gemm_ws = nullptr;
     int* gemm_counters = nullptr;
+    float* gemm_ws_side = nullptr;     // the same for GEMMs on side_stream (they may run concurrently)
+    int* gemm_counters_side = nullptr;
     bool launch_failed = false;
     float* keep_prefill = nullptr;
     float* keep_draft = nullptr;
@@ -173,9 +175,10 @@ struct dflash_ctx {
 
     Launch L() {
         Launch l{stream, &launches};
-        l.ws = gemm_ws;
+        const bool side = side_stream && stream == side_stream;
+        l.ws = side ? gemm_ws_side : gemm_ws;
         l.ws_bytes = GEMM_WS_BYTES;
-        l.counters = gemm_counters;
+        l.counters = side ? gemm_counters_side : gemm_counters;
         l.n_counters = GEMM_COUNTERS;
         l.err = errw;
         l.failed = &launch_failed;
@@ -308,11 +311,12 @@ dflash_status pack_layer(dflash_ctx* c, const dflash_layer_weights& w, LayerW& o
     if ((s = copy_rows(c, o.wqkv, qd, w.wk, kvd, d))) return s;
     if ((s = copy_rows(c, o.wqkv, qd + kvd, w.wv, kvd, d))) return s;
     if (c->cfg.dtype == DFLASH_DTYPE_BF16) {
-        // SwiGLU epilogue layout: tile j = gate rows [64j, 64j+64) then up rows [64j, 64j+64)
+        // SwiGLU epilogue layout: groups of 16 rows, gate rows [8g, 8g+8) then up rows [8g, 8g+8),
+        // so that a 128-row GEMM tile holds both halves of 64 features, eight TMEM lanes apart
         if (!w.w_gate || !w.w_up) return c->fail(DFLASH_E_INVAL, "a weight pointer is NULL");
-        const size_t blk = 64 * d * c->esz;
-        CUDA_TRY(c, cudaMemcpy2DAsync(o.wgu, 2 * blk, w.w_gate, blk, blk, F / 64, cudaMemcpyDeviceToDevice, c->stream));
-        CUDA_TRY(c, cudaMemcpy2DAsync((char*)o.wgu + blk, 2 * blk, w.w_up, blk, blk, F / 64, cudaMemcpyDeviceToDevice,
+        const size_t blk = 8 * d * c->esz;
+        CUDA_TRY(c, cudaMemcpy2DAsync(o.wgu, 2 * blk, w.w_gate, blk, blk, F / 8, cudaMemcpyDeviceToDevice, c->stream));
+        CUDA_TRY(c, cudaMemcpy2DAsync((char*)o.wgu + blk, 2 * blk, w.w_up, blk, blk, F / 8, cudaMemcpyDeviceToDevice,
                                       c->stream));
     } else {
         if ((s = copy_rows(c, o.wgu, 0, w.w_gate, F, d))) return s;
@@ -334,7 +338,12 @@ dflash_status check_device(dflash_ctx* c) {
     CUDA_TRY(c, cudaStreamSynchronize(c->stream));
     if (e) {
         CUDA_TRY(c, cudaMemsetAsync(c->errw, 0, 4, c->stream));
-        if (e & ERR_TIMEOUT) return c->fail(DFLASH_E_TIMEOUT, "a bounded device-side wait ran out (code %u)", e);
+        if (e & ERR_TIMEOUT) {
+            // a GEMM that stopped early may have left stream-K tile counters raised
+            CUDA_TRY(c, cudaMemsetAsync(c->gemm_counters, 0, (size_t)GEMM_COUNTERS * 4, c->stream));
+            CUDA_TRY(c, cudaMemsetAsync(c->gemm_counters_side, 0, (size_t)GEMM_COUNTERS * 4, c->stream));
+            return c->fail(DFLASH_E_TIMEOUT, "a bounded device-side wait ran out (code %u)", e);
+        }
         return c->fail(DFLASH_E_DEVICE_CHECK, "device-side check failed (code %u%s%s)", e,
                        (e & ERR_TOKEN_RANGE) ? ": token id outside [0, vocab)" : "",
                        (e & ERR_POSITION_RANGE) ? ": position beyond max_seq_len" : "");
@@ -403,14 +412,16 @@ struct Pass {
     // fp32 matrix x (row stride K).  bf16 blocks of <= 32 rows normalise inside the GEMM
     // (sums of squares from ss_in, left there by the kernel that wrote x); otherwise an
     // RMSNorm kernel writes the bf16/fp32 operand first.
+    // `fusable` false: the row sums of squares in ss_in may be stale (the rows were last written
+    // by a pass of more than 256 rows, whose persistent GEMM writes none), so normalise first.
     void normed_gemm(int kind, int rows, const float* x, const float* norm_w, const float* ss_in, const T* W, int N,
                      int K, float* C, int ldc, T* out, int ldo, unsigned long long* keys = nullptr,
-                     const QkvStoreEpi* qkv = nullptr, void* xbuf = nullptr) {
+                     const QkvStoreEpi* qkv = nullptr, void* xbuf = nullptr, bool fusable = true) {
         void* xn = xbuf ? xbuf : c->xn;
         Launch L = c->L();
         const double R = rows, es = c->esz;
         const double bytes = (double)N * K * es + R * K * 4 + (out ? R * ldo * es : R * N * 4.0);
-        const bool fused = is_bf16 && rows <= 32;
+        const bool fused = is_bf16 && rows <= 32 && fusable;
         if (!fused)
             timed(c, DFLASH_K_NORM, R * K * (4 + es), 0, [&] {
                 rmsnorm_rows<T>(L, x, K, norm_w, rows, K, c->cfg.rms_eps, (T*)xn, K);
@@ -630,7 +641,8 @@ struct Pass {
     // `block` > 0: draft rows, token ids of rows s*block+j (j >= 1) go to out[s*(block-1)+j-1].
     // `logits_to` set: the fp32 logits are written there (the sampled passes), else to
     // c->logits only when kept (bf16) or always (fp32, whose argmax reads them).
-    void head(int row0, int rows, const float* norm, int* out, float* keep, int block = 0, float* logits_to = nullptr) {
+    void head(int row0, int rows, const float* norm, int* out, float* keep, int block = 0, float* logits_to = nullptr,
+              bool fusable = true) {
         Launch L = c->L();
         const double R = rows, V = c->V;
         float* lg = logits_to ? logits_to : c->logits;
@@ -638,7 +650,8 @@ struct Pass {
             // head GEMM with the argmax in its epilogue (logits written only when needed)
             cudaMemsetAsync(c->keys, 0, (size_t)rows * sizeof(unsigned long long), c->stream);
             normed_gemm(DFLASH_K_GEMM_HEAD, rows, c->x + (size_t)row0 * c->d, norm, c->ss_x + row0,
-                        (const T*)c->head, c->V, c->d, (keep || logits_to) ? lg : nullptr, c->V, nullptr, 0, c->keys);
+                        (const T*)c->head, c->V, c->d, (keep || logits_to) ? lg : nullptr, c->V, nullptr, 0, c->keys,
+                        nullptr, nullptr, fusable);
             timed(c, DFLASH_K_ARGMAX, R * 8, 0, [&] { keys_to_ids(L, c->keys, rows, block, out); });
         } else {
             normed_gemm(DFLASH_K_GEMM_HEAD, rows, c->x + (size_t)row0 * c->d, norm, c->ss_x + row0,
@@ -670,7 +683,7 @@ struct Pass {
                 append_context(rows, c->row_seq, c->row_pos);
                 if (r0 + rows == P)
                     head(rows - 1, 1, c->final_norm, c->anchor + s,
-                         c->keep_prefill ? c->keep_prefill + (size_t)s * c->V : nullptr);
+                         c->keep_prefill ? c->keep_prefill + (size_t)s * c->V : nullptr, 0, nullptr, rows <= 256);
             }
             off += P;
         }
@@ -1083,6 +1096,8 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     ALLOC(c->attn_ws, ATTN_WS_BYTES);
     ALLOC(c->gemm_ws, GEMM_WS_BYTES);
     ALLOC(c->gemm_counters, (size_t)GEMM_COUNTERS * 4);
+    ALLOC(c->gemm_ws_side, GEMM_WS_BYTES);
+    ALLOC(c->gemm_counters_side, (size_t)GEMM_COUNTERS * 4);
     if (cfg->flags & DFLASH_FLAG_KEEP_LOGITS) {
         ALLOC(c->keep_prefill, (size_t)cfg->max_batch * V * 4);
         ALLOC(c->keep_draft, (size_t)rb * V * 4);
@@ -1097,6 +1112,7 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
         cudaMemsetAsync(c->dV, 0, (size_t)c->Ld * c->kv.layer_stride * esz, c->stream) != cudaSuccess ||
         cudaMemsetAsync(c->errw, 0, 16, c->stream) != cudaSuccess ||
         cudaMemsetAsync(c->gemm_counters, 0, (size_t)GEMM_COUNTERS * 4, c->stream) != cudaSuccess ||
+        cudaMemsetAsync(c->gemm_counters_side, 0, (size_t)GEMM_COUNTERS * 4, c->stream) != cudaSuccess ||
         cudaMemsetAsync(c->n, 0, (size_t)cfg->max_batch * 4, c->stream) != cudaSuccess) {
         c->fail(DFLASH_E_CUDA, "memset failed");
         return bail(DFLASH_E_CUDA);

@@ -32,10 +32,13 @@
 #include <cuda.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include <mutex>
 #include <unordered_map>
 
 #include "launch.h"
+#include "tcgen05.cuh"
 
 namespace dfl {
 
@@ -45,128 +48,7 @@ constexpr int BN = 128;          // weight rows per tile = UMMA M
 constexpr int BK = 64;           // K per stage: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
 constexpr int THREADS = 192;
-constexpr uint32_t WAIT_LIMIT = 1u << 26;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (i >= 1024) __nanosleep(128);
-    }
-    if (err) atomicOr(err, ERR_TIMEOUT);
-    return false;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-// 2-D tiled TMA load: coordinates {c0 = element along the contiguous dim, c1 = row}.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// UMMA shared-memory descriptor: K-major operand in the 128-byte swizzle
-// layout TMA produces (rows of 128 B, 8-row atoms 1024 B apart).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address, 16-byte units
-    d |= (uint64_t)1 << 16;                     // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: next 8-row atom
-    d |= (uint64_t)1 << 46;                     // descriptor version for tcgen05
-    d |= (uint64_t)2 << 61;                     // swizzle mode: 128 B
-    return d;
-}
-
-// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
-    return (1u << 4)                      // D format fp32
-           | (1u << 7)                    // A format bf16
-           | (1u << 10)                   // B format bf16
-           | ((uint32_t)(n >> 3) << 17)   // N / 8
-           | ((uint32_t)(BN >> 4) << 24); // M / 16
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-// 16 consecutive fp32 accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
+using namespace tc;
 
 struct QkvEpi {
     int q_tiles, n_kv;
@@ -183,23 +65,6 @@ struct QkvEpi {
     const int* row_pos;
 };
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// fp32 load from the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
-
 struct TcArgs {
     float* C;
     int ldc, M, N, K;
@@ -214,8 +79,9 @@ struct TcArgs {
     const float* ss_in;
     int ss_tiles, ss_ld;
     float eps;
-    // epilogue: 0 = fp32 C (=|+=); 1 = SwiGLU, tile rows [0,64) gate and [64,128) up of
-    // features 64*tile + i, written as bf16 silu(gate) * up to out[m * ldo + f]
+    // epilogue: 0 = fp32 C (=|+=); 1 = SwiGLU: tile rows 16g + i (i < 8) are the gate and
+    // rows 16g + 8 + i the up projection of feature 64*tile + 8g + i, written as bf16
+    // silu(gate) * up to out[m * ldo + f]
     int epi;
     void* out;
     int ldo;
@@ -243,25 +109,6 @@ struct Smem {
 
 // Sync of the four epilogue warps (warps 2..5) only.
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// Reduce 16 per-token values over the 32 lanes of a warp (v[t] = this lane's value of
-// token t) with 16 shuffles: each halving step keeps one half of the tokens and sends
-// the other half to the partner lane.  On return every lane holds the reduction of
-// token (lane >> 1).
-template <typename T, typename Op>
-__device__ __forceinline__ T transpose_reduce16(T (&v)[16], int lane, Op op) {
-#pragma unroll
-    for (int o = 16, c = 16; o >= 2; o >>= 1, c >>= 1) {
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < c / 2; ++i) {
-            const T send = upper ? v[i] : v[i + c / 2];
-            const T keep = upper ? v[i + c / 2] : v[i];
-            v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, o));
-        }
-    }
-    return op(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
-}
 
 template <int MT, int STAGES, bool NORM_A>
 __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
@@ -308,9 +155,9 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
         tmem_alloc(tmem_slot, TMEM_COLS);
         tmem_relinquish();
     }
-    tc_fence_before();
+    fence_before();
     __syncthreads();
-    tc_fence_after();
+    fence_after();
     const uint32_t tmem = *tmem_slot;
 
     pdl_trigger();  // the next kernel may start its own prologue now
@@ -356,7 +203,7 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(MT);
+            constexpr uint32_t idesc = idesc_bf16(BN, MT);
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % STAGES;
                 if (!mbar_wait(&full[s], (i / STAGES) & 1, a.err)) {
@@ -367,7 +214,7 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
                     ok = false;
                     break;
                 }
-                tc_fence_after();
+                fence_after();
                 const uint32_t sw = smem_u32(smem + s * S::STAGE_BYTES);
                 const uint32_t sx = sw + S::W_BYTES;
 #pragma unroll
@@ -464,7 +311,7 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
     if (epi_warp) {
         if (lane == 0) okw = mbar_wait(accf, 0, a.err) ? 1u : 0u;
         ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
-        tc_fence_after();
+        fence_after();
     }
 
     // Kernel arguments used per token, hoisted into registers once.
@@ -673,10 +520,12 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
             }
         }
         if (a.epi == 1) {
-            // thread e: feature r = e % 64 (gate row r, up row r + 64) of tokens j0 + e / 64, +2, ...;
+            // thread e: feature r = e % 64 of tokens j0 + e / 64, +2, ...; the tile holds gate and
+            // up rows in alternating groups of eight (gate of feature r at row gr, its up at gr + 8);
             // four tokens per iteration as independent chains (one warp per scheduler here)
             const int e = threadIdx.x - 64;
             const int r = e & 63;
+            const int gr = ((r >> 3) << 4) | (r & 7);
             const int f = 64 * nt + r;
             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + f;
             const size_t ldo = (size_t)a.ldo;
@@ -690,8 +539,8 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
                     float gv[4], uv[4];
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        gv[t] = xch[(j + 2 * t) * BN + r];
-                        uv[t] = xch[(j + 2 * t) * BN + r + 64];
+                        gv[t] = xch[(j + 2 * t) * BN + gr];
+                        uv[t] = xch[(j + 2 * t) * BN + gr + 8];
                     }
 #pragma unroll
                     for (int t = 0; t < 4; ++t)
@@ -699,99 +548,20 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
                 }
                 for (; j < jend; j += 2)
                     out[(size_t)(m0 + j) * ldo] =
-                        __float2bfloat16_rn(swiglu(xch[j * BN + r], xch[j * BN + r + 64]));
+                        __float2bfloat16_rn(swiglu(xch[j * BN + gr], xch[j * BN + gr + 8]));
             }
         }
     }
 
-    tc_fence_before();
+    fence_before();
     __syncthreads();
     if (warp == 1) {
-        tc_fence_after();
+        fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-struct MapKey {
-    const void* ptr;
-    long long rows, cols, ld;
-    int box_rows, f32;
-    bool operator==(const MapKey& o) const {
-        return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && box_rows == o.box_rows && f32 == o.f32;
-    }
-};
-struct MapKeyHash {
-    size_t operator()(const MapKey& k) const {
-        size_t h = std::hash<const void*>()(k.ptr);
-        h ^= std::hash<long long>()(k.rows * 1000003LL + k.cols) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
-        h ^= std::hash<long long>()(k.ld * 131 + k.box_rows * 2 + k.f32) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
-        return h;
-    }
-};
-
-// Tensor map of a row-major matrix [rows, cols] (row stride ld elements), box
-// [box_rows, 64]: bf16 with 128-byte swizzle (MMA operands), or fp32 without
-// swizzle (raw residual tiles); out-of-range elements read as zero.
-bool make_map(CUtensorMap* out, const void* ptr, long long rows, long long cols, long long ld, int box_rows,
-              bool f32 = false) {
-    static std::mutex mu;
-    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-    const MapKey key{ptr, rows, cols, ld, box_rows, f32 ? 1 : 0};
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) {
-        *out = it->second;
-        return true;
-    }
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const int esz = f32 ? 4 : 2;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUtensorMap m;
-    CUresult r = fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    f32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return false;
-    if (cache.size() > 65536) cache.clear();
-    cache.emplace(key, m);
-    *out = m;
-    return true;
-}
-
-int sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
-    }
-    return n;
-}
-
 // Split count (cluster size): the largest power of two that keeps the grid within
 // one wave of `slots` CTAs.  The cluster reduction of the [MT x 128] fp32 partial
 // tile grows with MT, so wider tiles split less: up to 8 ways for tiles of <= 32
@@ -837,6 +607,88 @@ bool launch_tc(const Launch& L, const CUtensorMap& mw, const CUtensorMap& mx, Tc
 }
 
 }  // namespace
+
+namespace tc {
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void* ptr;
+    long long rows, cols, ld;
+    int box_rows, f32;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && box_rows == o.box_rows && f32 == o.f32;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        size_t h = std::hash<const void*>()(k.ptr);
+        h ^= std::hash<long long>()(k.rows * 1000003LL + k.cols) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+        h ^= std::hash<long long>()(k.ld * 131 + k.box_rows * 2 + k.f32) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+        return h;
+    }
+};
+}  // namespace
+
+bool make_map(CUtensorMap* out, const void* ptr, long long rows, long long cols, long long ld, int box_rows,
+              bool f32) {
+    static std::mutex mu;
+    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+    const MapKey key{ptr, rows, cols, ld, box_rows, f32 ? 1 : 0};
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+        *out = it->second;
+        return true;
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int esz = f32 ? 4 : 2;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUtensorMap m;
+    CUresult r = fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    f32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    if (cache.size() > 65536) cache.clear();
+    cache.emplace(key, m);
+    *out = m;
+    return true;
+}
+
+int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+}  // namespace tc
 
 // bf16 GEMM on the tensor cores.  Returns false when a tensor map cannot be
 // built (the caller reports the error); nothing is launched in that case.
@@ -910,6 +762,20 @@ bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W,
     }
     if (a.ss_out && a.epi != 0) return false;
     if (a.epi == 2 && !a.keys) return false;
+    // Passes of more than 256 rows (no row sums of squares there: the fused norm that reads
+    // them serves blocks of at most 32 rows).  Measured at 512 rows on Qwen3-8B shapes: when the
+    // 128 x 256 tiles fill at least one wave of the GPU the persistent kernel with whole tiles
+    // wins (its epilogue overlaps the next tile's main loop); under one wave it wins only for long
+    // K, with stream-K balancing (W_c, down); short-K GEMMs under one wave (QKV, O, context K/V)
+    // keep the per-tile kernel below.
+    if (!norm_a && a.epi != 3 && M > 256) {
+        const int p_mtiles = (M + 255) / 256, p_ntiles = (N + BN - 1) / BN, KB = (K + BK - 1) / BK;
+        const long long T = (long long)p_mtiles * p_ntiles;
+        const int G = std::max(1, sm_count() / p_mtiles) * p_mtiles;
+        if (T >= G || KB >= 128)
+            return gemm_tc_persistent(L, A, lda, a_rows, W, M, N, K, C, ldc, accumulate, a.epi, a.out, a.ldo, a.keys,
+                                      /*stream_k=*/T < G);
+    }
     const int m_tiles = (M + MT - 1) / MT;
     if (norm_a) {
         if (MT == 16) return launch_tc<16, 4, true>(L, mw, mx, a, m_tiles);

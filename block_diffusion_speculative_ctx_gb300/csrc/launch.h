@@ -13,9 +13,9 @@ namespace dfl {
 struct Launch {
     cudaStream_t stream;
     long long* launches;        // incremented once per kernel launch (may be null)
-    float* ws = nullptr;        // split-K partial tiles (null: no split-K)
+    float* ws = nullptr;        // stream-K partial tiles (null: whole tiles only)
     size_t ws_bytes = 0;
-    int* counters = nullptr;    // split-K tile counters, zero between launches
+    int* counters = nullptr;    // stream-K tile counters, zero between launches
     int n_counters = 0;
     uint32_t* err = nullptr;    // device error word
     bool* failed = nullptr;     // host flag: a launch could not be prepared
@@ -69,8 +69,9 @@ void gemm(const Launch& L, const T* A, int lda, const T* W, int M, int N, int K,
 //  - x_f32 set: the A operand is the fp32 matrix x [M, K] (row stride ldx) normalised on
 //    the fly, A = bf16(x * rstd[m] * norm_w[k]) with rstd[m] = 1/sqrt(sum_t ss_in[t*ss_ld+m]/K + eps)
 //    (blocks of at most 32 rows); the A/lda arguments are ignored;
-//  - epi 1: SwiGLU; W holds, per 128-row tile j, gate rows [64j, 64j+64) then up rows
-//    [64j, 64j+64); out[m * ldo + f] = bf16(silu(gate_f) * up_f); C is unused;
+//  - epi 1: SwiGLU; W holds gate and up rows in alternating groups of eight (rows 16g..16g+7
+//    are gate rows 8g..8g+7, rows 16g+8..16g+15 the matching up rows); out[m * ldo + f] =
+//    bf16(silu(gate_f) * up_f); C is unused;
 //  - ss_out set (epi 0): ss_out[tile * ss_ld + m] = sum over the tile's 128 columns of C[m][n]^2
 //    after the update, for the next fused norm;
 //  - epi 2: row argmax: keys[m] = max_n argmax_key(C[m][n], n) by atomicMax (keys start at zero; C is
@@ -109,9 +110,17 @@ struct GemmEpi {
 };
 
 // tcgen05 GEMM for bf16; false when it could not be launched (tensor map encode
-// failed or an unsupported option combination).
+// failed or an unsupported option combination).  Passes of more than 256 rows without
+// the fused norm or the q/k/v epilogue may run on the persistent kernel (gemm_persistent.cu),
+// which writes no row sums of squares (ss_out) and uses L.ws / L.counters for stream-K
+// partial tiles.
 bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W, int M, int N, int K, float* C,
              int ldc, bool accumulate, const GemmEpi* ep = nullptr);
+// The persistent kernel itself: epi 0 (C =|+=), 1 (SwiGLU to out), 2 (row argmax keys, C
+// written when non-null); stream_k false: whole 128 x 256 tiles only.
+bool gemm_tc_persistent(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W, int M, int N, int K,
+                        float* C, int ldc, bool accumulate, int epi, void* out, int ldo, unsigned long long* keys,
+                        bool stream_k);
 
 // ---- row kernels
 // Rows of the embedding table; with ss_out, also the per-128-column-tile sums of

@@ -114,6 +114,14 @@ def _build() -> dict:
     # Prompt longer than one prefill chunk (2048 rows): chunked causal prefill.
     w["small_bf16_long"] = w["small_bf16"].with_(name="small_bf16_long", prompt_lens=(2100, 300),
                                                  prompt_seed=11)
+    # Batch 20: 320-row draft and verify passes (two 256-token tiles) with an FFN of 8192 and a
+    # vocabulary of 40000, so that the round's gate/up and head GEMMs fill a wave of 128 x 256
+    # tiles (the persistent kernel, whole tiles) and its down projection has K = 8192 (the
+    # persistent kernel with stream-K pieces summed across CTAs).
+    w["small_bf16_b20"] = w["small_bf16"].with_(
+        name="small_bf16_b20", batch=20, ffn=8192, vocab=40000,
+        prompt_lens=(37, 100, 5, 64, 19, 130, 250, 8, 77, 41, 300, 3, 58, 90, 16, 121, 29, 66, 200, 11),
+        prompt_seed=13)
     # LLaMA-style small model without target QK-norm, batch 4.
     w["small_bf16_llama"] = Workload(
         name="small_bf16_llama", dtype="bf16", vocab=3001, d_model=512, n_heads=4, n_kv_heads=1,

@@ -173,6 +173,13 @@ def test_small_bf16_llama_batch12_stepwise():
     assert run_stepwise("small_bf16_llama_b12", rounds=3) >= 18    # of 12 x 3
 
 
+def test_small_bf16_batch20_persistent_gemm_stepwise():
+    # 320 block rows per pass: gate/up (SwiGLU) and the head (argmax, logits kept) run on the
+    # persistent kernel with whole tiles, the down projection (residual add, K = 8192) with
+    # stream-K pieces summed across CTAs
+    assert run_stepwise("small_bf16_b20", rounds=3) >= 20    # of 20 x 3
+
+
 @pytest.mark.parametrize("block", [8, 10])
 def test_small_bf16_block_sizes_8_and_10(block):
     # the LLaMA setup's B = 10 and the smaller block suggested under load
@@ -298,10 +305,12 @@ def _final_residual(m, prompt, block):
     return x
 
 
-def test_graph_replay_matches_eager_launches():
+@pytest.mark.parametrize("name", ["small_bf16_llama", "small_bf16_b20"])
+def test_graph_replay_matches_eager_launches(name):
     """Rounds replayed from captured CUDA graphs give bit-identical results to
-    the same rounds launched kernel by kernel."""
-    w = configs.get("small_bf16_llama")
+    the same rounds launched kernel by kernel (at batch 20 through the persistent
+    stream-K GEMM, whose split tiles are summed in a fixed order)."""
+    w = configs.get(name)
     prompts = synth.prompts(w)
     b, B = len(prompts), w.block_size
     props = [synth.uniform_ints(500 + r, 0x33, b * (B - 1), w.vocab).reshape(b, B - 1).astype(np.int32)
