@@ -679,7 +679,9 @@ struct Pass {
                                             c->stream));
                 fill_prefill_rows(L, s, r0, rows, c->row_seq, c->row_pos);
                 embed_rows<T>(L, c->tokens, (const T*)c->embed, c->V, c->d, rows, c->x, c->errw, c->ss_x, c->R);
-                layers(true, rows, c->row_seq, c->row_pos, 64 / g, r0 + rows, true, (double)(r0 + rows));
+                // bf16, head_dim 128: query groups of 128 vectors for the tcgen05 prefill attention
+                const int gr = (is_bf16 && c->hd == 128 && 128 % g == 0) ? 128 / g : 64 / g;
+                layers(true, rows, c->row_seq, c->row_pos, gr, r0 + rows, true, (double)(r0 + rows));
                 append_context(rows, c->row_seq, c->row_pos);
                 if (r0 + rows == P)
                     head(rows - 1, 1, c->final_norm, c->anchor + s,

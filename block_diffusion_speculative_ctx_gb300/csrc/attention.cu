@@ -280,7 +280,9 @@ void attention<float>(const Launch& L, const AttnParams& p) {
         run<float, 64>(L, p);
 }
 
-// bf16 storage: the tensor-core kernel (attention_mma.cu).
+// bf16 storage: causal prefill chunks with 128-vector query groups run on tcgen05
+// (attention_prefill.cu); the round's blocks (and anything else) on mma.sync
+// (attention_mma.cu).
 template <>
 void attention<bf16>(const Launch& L, const AttnParams& p) {
     static int sms = 0;
@@ -289,6 +291,10 @@ void attention<bf16>(const Launch& L, const AttnParams& p) {
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 148;
+    }
+    if (!p.seq_len && p.seq_div == 0 && p.hd == 128 && p.group_rows * (p.H / p.Hkv) == 128) {
+        if (!attention_prefill_tc(L, p)) L.fail();
+        return;
     }
     attention_mma(L, p, sms);
 }

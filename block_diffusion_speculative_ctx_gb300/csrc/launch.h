@@ -199,8 +199,12 @@ struct AttnParams {
 };
 template <typename T>
 void attention(const Launch& L, const AttnParams& p);
-// bf16 path of attention(): tensor cores (mma.sync), cluster-merged key splits.
+// bf16 path of attention(): tensor cores (mma.sync), cluster-merged key splits; query groups
+// of at most 64 vectors (group_rows * H / H_kv <= 64).
 void attention_mma(const Launch& L, const AttnParams& p, int sms);
+// Causal prefill attention on tcgen05 (attention_prefill.cu): head_dim 128, query groups of
+// exactly 128 vectors (group_rows * H / H_kv == 128); false when it cannot be launched.
+bool attention_prefill_tc(const Launch& L, const AttnParams& p);
 
 // ---- temperature sampling (sampling.cu)
 // Draft rows s*B + j (j = 1..B-1) of dlogits [batch*B, V]: dstat[row] = (max, sum exp((l - max)/T)),

@@ -115,14 +115,29 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both operands K-major,
-// M = m (64 or 128), N = n (multiple of 16 up to 256).
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-    return (1u << 4)                      // D format fp32
-           | (1u << 7)                    // A format bf16
-           | (1u << 10)                   // B format bf16
-           | ((uint32_t)(n >> 3) << 17)   // N / 8
-           | ((uint32_t)(m >> 4) << 24);  // M / 16
+// General form: leading and stride byte offsets given.  For an MN-major operand in the
+// 128-byte swizzle (rows of 64 consecutive MN elements, one row per K index) the leading
+// byte offset is the stride between 64-element atoms along MN and the stride byte offset
+// the stride between 8-row groups along K.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, A K-major, B K-major (or
+// MN-major when b_mn_major), M = m (64 or 128), N = n (multiple of 16 up to 256).
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major = false) {
+    return (1u << 4)                                 // D format fp32
+           | (1u << 7)                               // A format bf16
+           | (1u << 10)                              // B format bf16
+           | ((b_mn_major ? 1u : 0u) << 16)          // B major-ness
+           | ((uint32_t)(n >> 3) << 17)              // N / 8
+           | ((uint32_t)(m >> 4) << 24);             // M / 16
 }
 
 // D (TMEM) (+)= A (smem) . B (smem)^T, issued by one thread.
@@ -171,6 +186,20 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
                    "+r"(r[15])
                  :
                  : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane stored from registers (waits).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+        "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+        "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
