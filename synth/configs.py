@@ -114,6 +114,15 @@ def _build() -> dict:
     # Prompt longer than one prefill chunk (2048 rows): chunked causal prefill.
     w["small_bf16_long"] = w["small_bf16"].with_(name="small_bf16_long", prompt_lens=(2100, 300),
                                                  prompt_seed=11)
+    # Long injected context at small width: prompts of 8200-8448 tokens (4 prefill chunks of 2048
+    # rows and a ragged one), so the draft attention walks up to 133 context pages per KV head (8+
+    # key tiles per cluster rank) and the verify attention as many, as in the 8K benchmark workload.
+    # (three sequences: a bf16 near-tie retires one sequence from the comparison, not the test)
+    w["small_bf16_long8k"] = Workload(
+        name="small_bf16_long8k", dtype="bf16", vocab=5000, d_model=1024, n_heads=8, n_kv_heads=2, head_dim=128,
+        ffn=2816, target_layers=2, target_qk_norm=True, rope_theta=1e6, draft_layers=1, block_size=16,
+        ctx_layer_ids=(0, 1), batch=3, prompt_lens=(8448, 8300, 8200), max_new_tokens=48, norm_std=0.1,
+        weight_seed=14, prompt_seed=15)
     # Batch 20: 320-row draft and verify passes (two 256-token tiles) with an FFN of 8192 and a
     # vocabulary of 40000, so that the round's gate/up and head GEMMs fill a wave of 128 x 256
     # tiles (the persistent kernel, whole tiles) and its down projection has K = 8192 (the

@@ -8,9 +8,13 @@ stay on the host for the fp64 oracle.
 * qwen3_8b_b1_p512: full prefill, first token, prefill logits, draft-context
   K/V, then two rounds (draft logits and tokens, verify logits and posterior,
   acceptance, bonus, committed length).
-* llama31_8b_b8_p1024 / qwen3_8b_c32_ragged: the same for one sequence of the
-  batch (the shortest one for the ragged batch); every sequence is checked for
-  the structural invariants (lengths, acceptance range).
+* llama31_8b_b8_p1024 / qwen3_8b_c32_ragged: the same for two sequences of the
+  batch (the first two; the two shortest of the ragged batch); every sequence is
+  checked for the structural invariants (lengths, acceptance range).
+* In the first round each checked sequence is proposed the target's own next
+  token (one greedy oracle step from its prefilled cache) followed by random
+  tokens, so that round accepts a draft: the context append of several rows and
+  the rollback after a partial acceptance are compared at full size.
 * qwen3_8b_b1_p8192: the context K/V of the first 64 prompt positions (a
   causal prefill of those 64 tokens gives the same values) and the invariants
   of two rounds.
@@ -23,8 +27,10 @@ like sqrt(depth).  Each test therefore measures that storage-noise envelope on
 the prefill (bf16-storage oracle vs pure fp64 oracle) and requires the GPU to
 lie within 1.5x of it, and never looser than the shallow tolerances: a wrong
 layer, weight or position is off by O(1), far outside.  Tokens may differ only
-where the oracle's top-2 margin is below the logit tolerance.  Proposals are
-fixed synthetic tokens, the same on both sides.
+where the oracle's top-2 margin is below the logit tolerance.  Every logit
+comparison also prints whether it meets the stated bf16 bounds themselves
+(max-abs 5e-2, rel-L2 1e-2).  Proposals are fixed synthetic tokens (after the
+planted first token), the same on both sides.
 """
 import gc
 
@@ -70,6 +76,9 @@ class Envelope:
     def logits(self, gpu, ora, what):
         mx = float(np.abs(gpu - ora).max())
         rl = _rel_l2(gpu, ora)
+        stated = mx <= LOGIT_TOL and rl <= REL_TOL
+        print(f"{what}: max-abs {mx:.3g}, rel-L2 {rl:.3g}; stated bounds (5e-2, 1e-2) "
+              f"{'met' if stated else 'not met'}; envelope ({self.logit:.3g}, {self.rel:.3g})")
         assert mx <= self.logit and rl <= self.rel, f"{what}: max-abs {mx:.3g} (tol {self.logit:.3g}), " \
                                                     f"rel-L2 {rl:.3g} (tol {self.rel:.3g})"
 
@@ -118,6 +127,7 @@ def _run(w, data, check_seqs, rounds, oracle_prefix=None):
         lens0 = sess.lengths()
         np.testing.assert_array_equal(lens0, np.array(w.prompt_lens))
         states = {}
+        env = None
         for s in check_seqs:
             if oracle_prefix:
                 # causal: the first `oracle_prefix` positions do not see the rest of the prompt
@@ -130,20 +140,30 @@ def _run(w, data, check_seqs, rounds, oracle_prefix=None):
                     assert _rel_l2(v, st.dcache.v[l]) < env.cache
                 continue
             st = spec.prefill(m, prompts[s])
-            env = Envelope(st, spec.prefill(data.oracle(w, act_round=False), prompts[s]))
-            print(f"seq {s}: envelope logits {env.logit:.3g} rel {env.rel:.3g} cache {env.cache:.3g}")
+            if env is None:   # the storage-noise envelope of the first checked sequence serves the test
+                env = Envelope(st, spec.prefill(data.oracle(w, act_round=False), prompts[s]))
+                print(f"seq {s}: envelope logits {env.logit:.3g} rel {env.rel:.3g} cache {env.cache:.3g}")
             env.logits(plog[s], st.first_logits, "prefill logits")
             if not _tok_ok(first[s:s + 1], st.first_logits[None], env.logit):
                 continue                                    # exempt near-tie: streams differ from here
             for l in (0, w.draft_layers - 1):
                 assert _rel_l2(sess.cache("draft", "k", s, l), st.dcache.k[l]) < env.cache
                 assert _rel_l2(sess.cache("draft", "v", s, l), st.dcache.v[l]) < env.cache
-            states[s] = (st, env)
+            # the target's next token after the first one: one greedy step of the oracle from a
+            # copy of the prefilled cache (planted as the first draft of round 0)
+            cache = st.tcache.copy()
+            lg1, _ = m.target_forward([st.anchor], cache)
+            nxt = int(om.argmax_lowest(lg1)[0])
+            states[s] = (st, env, nxt, float(spec.top2_margin(lg1)[0]))
         compared = 0
+        accepted_any = False
         for r in range(rounds):
             drafts = sess.draft_block()
             dlog = sess.logits("draft")
             prop = synth.uniform_ints(900 + r, 0x66, b * (B - 1), w.vocab).reshape(b, B - 1).astype(np.int32)
+            if r == 0:
+                for s, (st, env_s, nxt, _) in states.items():
+                    prop[s, 0] = nxt
             n_before = sess.lengths().copy()
             acc, bon = sess.verify(prop)
             vlog = sess.logits("verify")
@@ -152,7 +172,7 @@ def _run(w, data, check_seqs, rounds, oracle_prefix=None):
             assert np.all((acc >= 0) & (acc <= B - 1))
             np.testing.assert_array_equal(lens, n_before + acc + 1)
             np.testing.assert_array_equal(bon, post[np.arange(b), acc])
-            for s, (st, env) in list(states.items()):
+            for s, (st, env, nxt, m1) in list(states.items()):
                 od, odl = spec.draft(m, st)
                 env.logits(dlog[s], odl, f"round {r} seq {s} draft logits")
                 _tok_ok(drafts[s], odl[1:], env.logit)
@@ -164,26 +184,32 @@ def _run(w, data, check_seqs, rounds, oracle_prefix=None):
                     del states[s]                           # exempt near-tie changed the stream
                     continue
                 assert lens[s] == st.committed
+                if r == 0 and m1 >= env.logit:
+                    assert rd.accepted >= 1, "the planted true next token was not accepted"
+                accepted_any |= rd.accepted >= 1
                 compared += 1
-        print(f"{w.name}: sequences checked {len(check_seqs)}, rounds with equal acceptance {compared}")
-        return compared
+        print(f"{w.name}: sequences checked {len(check_seqs)}, rounds with equal acceptance {compared}, "
+              f"a draft accepted: {accepted_any}")
+        return compared, accepted_any
     finally:
         sess.close()
         gc.collect()
 
 
 def test_qwen3_8b_b1_p512(qwen):
-    _run(configs.get("qwen3_8b_b1_p512"), qwen, [0], rounds=2)
+    compared, accepted = _run(configs.get("qwen3_8b_b1_p512"), qwen, [0], rounds=2)
+    assert compared == 0 or accepted
 
 
 def test_qwen3_8b_b1_p8192_first_positions(qwen):
     _run(configs.get("qwen3_8b_b1_p8192"), qwen, [0], rounds=2, oracle_prefix=64)
 
 
-def test_qwen3_8b_c32_ragged_shortest_sequence(qwen):
+def test_qwen3_8b_c32_ragged_two_shortest_sequences(qwen):
     w = configs.get("qwen3_8b_c32_ragged")
-    s = int(np.argmin(w.prompt_lens))
-    _run(w, qwen, [s], rounds=2)
+    seqs = [int(i) for i in np.argsort(w.prompt_lens, kind="stable")[:2]]
+    compared, accepted = _run(w, qwen, seqs, rounds=2)
+    assert compared == 0 or accepted
 
 
 def test_llama31_8b_b8_p1024_first_sequence(qwen):
@@ -193,7 +219,8 @@ def test_llama31_8b_b8_p1024_first_sequence(qwen):
     gc.collect()
     data = ModelData(configs.get("llama31_8b_b8_p1024"))
     try:
-        _run(configs.get("llama31_8b_b8_p1024"), data, [0], rounds=2)
+        compared, accepted = _run(configs.get("llama31_8b_b8_p1024"), data, [0, 1], rounds=2)
+        assert compared == 0 or accepted
     finally:
         data.dev.clear()
         data.host.clear()

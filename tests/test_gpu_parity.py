@@ -50,6 +50,18 @@ def _tokens_match(gpu_tok, ora_logits, bf16, near=BF16_MARGIN):
     return int(bad[0]) if len(bad) else -1
 
 
+def _greedy_stream(m, st, n):
+    """The target's plain greedy continuation (first token first) from a prefilled oracle state,
+    one single-token causal step at a time on a copy of its cache: the same computation as
+    spec.ar_generate without repeating the prefill."""
+    cache = st.tcache.copy()
+    out = [int(st.anchor)]
+    while len(out) < n:
+        lg, _ = m.target_forward([out[-1]], cache)
+        out.append(int(om.argmax_lowest(lg)[0]))
+    return np.array(out, dtype=np.int64)
+
+
 def _rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
@@ -73,9 +85,9 @@ def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), schedule=None, **wkw)
     m = om.Model(w)
     prompts = synth.prompts(w)
     n_ar = 1 + rounds * w.block_size + 1
-    streams = [spec.ar_generate(m, p, n_ar)[0] for p in prompts]
-    props = [spec.planted_proposer(s, taus, w.vocab) for s in streams]
     states = [spec.prefill(m, p) for p in prompts]
+    streams = [_greedy_stream(m, st, n_ar) for st in states]
+    props = [spec.planted_proposer(s, taus, w.vocab) for s in streams]
     alive = [True] * len(states)
     sess = _session(w, keep_logits=True, max_seq_len=max(w.prompt_lens) + (rounds + 2) * w.block_size + 8)
     try:
@@ -171,6 +183,14 @@ def test_small_bf16_llama_batch4_stepwise():
 def test_small_bf16_llama_batch12_stepwise():
     # 192 block rows per pass: GEMM tiles of 256 tokens, tokens 128..191 in the tile's second half
     assert run_stepwise("small_bf16_llama_b12", rounds=3) >= 18    # of 12 x 3
+
+
+def test_small_bf16_long_context_8k_stepwise():
+    # 8448 context entries: the draft attention over [context ; block] and the verify attention
+    # each walk 133 pages per KV head (8+ key tiles per rank of a 16-CTA cluster); the prefill
+    # runs 5 chunks through the tcgen05 causal attention.  Draft and verify logits every round at
+    # the stated bf16 tolerances, accepted drafts planted from the oracle's own greedy stream.
+    assert run_stepwise("small_bf16_long8k", rounds=3, taus=(1, 3, 2)) >= 3     # of 3 x 3
 
 
 def test_small_bf16_batch20_persistent_gemm_stepwise():
