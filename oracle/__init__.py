@@ -12,7 +12,8 @@ spec     prefill / draft / verify / accept loop, plain AR greedy decode,
          planted proposals that fix the number of accepted drafts.
 metrics  acceptance length, cycle latency, speedup, memory accounting,
          context-layer selection.
-sampling rounds at temperature T > 0: draft laws, proposals drawn by
+sampling rounds at temperature T > 0: draft laws (optionally filtered by
+         top-k / top-p, the same setting for both laws), proposals drawn by
          inverse CDF from caller-supplied uniforms, acceptance min(1, p/q),
          residual resampling, bonus draw.
 training the drafter's training forward (loss value): features of the clean
@@ -41,6 +42,11 @@ mathematics, not against this code):
   totals, eq. 8 (the emitted token has the target's law) by seeded Monte
   Carlo, which also rejects resampling from the target on rejection, and the
   T -> 0 limit equal to the greedy round;
+* top-k / top-p: closed forms on hand-made laws (temperature first, top-p on
+  the renormalised top-k law, the strict "mass before < p" rule, ties in
+  increasing id), the kept sets by brute force over subsets, a filtered
+  residual known in closed form, top-k = 1 equal to the greedy round, and the
+  whole round emitting the filtered target law (seeded Monte Carlo);
 * training: the packed block-sparse pass equals one pass per anchor, a block
   equals the inference draft pass with the same context and anchor token, no
   block sees a token at or after its anchor (or another block), the review's

@@ -16,7 +16,17 @@ Readings where the pages leave the step open:
 - laws: q_j = softmax(draft logits of block row j / T) for the mask rows
   j = 1..B-1; p_j = softmax(verify logits of block row j / T), the target's
   law for the token after block row j (so proposal j, block row j + 1, is
-  accepted or rejected under p_j); top-p / top-k are not applied;
+  accepted or rejected under p_j);
+- top-k / top-p ("Paper vs code", "Sampling rule": they apply to both the
+  draft and the target distributions): one setting (k, p) filters every law
+  q_j and p_j after the temperature.  Tokens are ranked by probability,
+  highest first, equal probabilities (equal logits) in increasing token id;
+  top-k keeps the first min(k, V) of them (k = 0: all); top-p then keeps,
+  under the top-k law renormalised, each token whose mass ranked strictly
+  before it is below p (the smallest ranked prefix whose mass reaches p;
+  p = 1: all); the kept tokens' probabilities are renormalised.  Eq. 6-8
+  then hold for the filtered laws, so the emitted token has the filtered
+  target law;
 - every draw is an inverse-CDF lookup with a caller-supplied uniform
   u in [0, 1): the lowest index z whose cumulative weight exceeds u times the
   total weight (the method's random numbers are inputs, so both sides of a
@@ -43,6 +53,35 @@ def softmax_t(logits: np.ndarray, T: float) -> np.ndarray:
     z = z - z.max(axis=-1, keepdims=True)
     e = np.exp(z)
     return e / e.sum(axis=-1, keepdims=True)
+
+
+def rank_order(logits: np.ndarray) -> np.ndarray:
+    """Token ids by decreasing logit (= decreasing probability at any T > 0),
+    equal logits in increasing id."""
+    l = np.asarray(logits, dtype=np.float64)
+    return np.lexsort((np.arange(l.shape[-1]), -l))
+
+
+def filter_law(logits: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0) -> np.ndarray:
+    """softmax(logits / T) of one row, restricted to its top-k tokens, then to
+    the top-p prefix of that renormalised law, and renormalised."""
+    pi = softmax_t(logits, T)
+    V = pi.shape[-1]
+    order = rank_order(logits)
+    kept = order[: top_k] if 0 < top_k < V else order
+    if top_p < 1.0:
+        w = pi[kept] / pi[kept].sum()
+        before = np.cumsum(w) - w                     # mass ranked strictly before each token
+        kept = kept[before < top_p]
+    out = np.zeros(V)
+    out[kept] = pi[kept]
+    return out / out.sum()
+
+
+def filter_laws(logits: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0) -> np.ndarray:
+    """filter_law of every row of a [rows, V] array."""
+    lg = np.atleast_2d(logits)
+    return np.stack([filter_law(r, T, top_k, top_p) for r in lg])
 
 
 def sample_inverse_cdf(weights: np.ndarray, u: float) -> int:
@@ -74,27 +113,30 @@ def speculative_step(p: np.ndarray, q: np.ndarray, u_draft: float, u_acc: float,
     return (sample_inverse_cdf(r, u_emit) if Z > 0.0 else sample_inverse_cdf(p, u_emit)), False
 
 
-def draft_sampled(model: Model, st: SeqState, T: float, u_draft: np.ndarray):
-    """Algorithm 1 steps 2-3: the drafter's laws q_1..q_{B-1} and the proposals
-    drawn from them.  Returns (proposals [B-1], q [B-1, V], draft logits [B, V])."""
+def draft_sampled(model: Model, st: SeqState, T: float, u_draft: np.ndarray, top_k: int = 0,
+                  top_p: float = 1.0):
+    """Algorithm 1 steps 2-3: the drafter's laws q_1..q_{B-1} (filtered by
+    top-k / top-p) and the proposals drawn from them.
+    Returns (proposals [B-1], q [B-1, V], draft logits [B, V])."""
     lg = model.draft_forward(st.anchor, st.dcache)
-    q = softmax_t(lg[1:], T)
+    q = filter_laws(lg[1:], T, top_k, top_p) if lg.shape[0] > 1 else softmax_t(lg[1:], T)
     y = np.array([sample_inverse_cdf(q[j], float(u_draft[j])) for j in range(q.shape[0])], dtype=np.int64)
     return y, q, lg
 
 
 def verify_sampled(model: Model, st: SeqState, proposal, q: np.ndarray, T: float, u_acc: np.ndarray,
-                   u_emit: float, keep_logits: bool = False) -> Round:
+                   u_emit: float, keep_logits: bool = False, top_k: int = 0, top_p: float = 1.0) -> Round:
     """Algorithm 1 steps 4-10 with eq. 6-8: scan proposals left to right under
     the surviving prefix; at the first rejection emit a residual draw, else the
-    bonus draw from p_{B-1}.  Caches keep the anchor and accepted rows."""
+    bonus draw from p_{B-1}.  The target laws p_j are filtered by top-k /
+    top-p like the drafter's.  Caches keep the anchor and accepted rows."""
     c = model.cfg
     n0 = st.committed
     proposal = np.asarray(proposal, dtype=np.int64)
     assert proposal.shape == (c.block_size - 1,)
     block = np.concatenate([[st.anchor], proposal])
     lg, sel = model.target_forward(block, st.tcache)
-    p = softmax_t(lg, T)
+    p = filter_laws(lg, T, top_k, top_p)
     a = 0
     for j in range(c.block_size - 1):
         y = int(proposal[j])
