@@ -280,12 +280,13 @@ def run_sampled(args, local):
     w = workload_of(args)
     B, b, T = w.block_size, w.batch, args.temperature
     K, W = args.steps, args.warmup
-    sess = Session(w, max_seq_len=max(w.prompt_lens) + (K + W + 4) * B)
+    sess = Session(w, max_seq_len=max(w.prompt_lens) + (K + W + 8) * B)
+    sess.set_sampling_filter(args.top_k, args.top_p)
     sess.prefill(synth.prompts(w))
     g = torch.Generator(device="cuda")
     g.manual_seed(1234)
-    ud = torch.rand((K + W, b, max(B - 1, 1)), generator=g, device="cuda")
-    uv = torch.rand((K + W, b, B), generator=g, device="cuda")
+    ud = torch.rand((K + W + 3, b, max(B - 1, 1)), generator=g, device="cuda")
+    uv = torch.rand((K + W + 3, b, B), generator=g, device="cuda")
     drafts = torch.zeros((b, max(B - 1, 1)), dtype=torch.int32, device="cuda")
     acc = torch.zeros((K + W, b), dtype=torch.int32, device="cuda")
     emit = torch.zeros((b,), dtype=torch.int32, device="cuda")
@@ -306,12 +307,23 @@ def run_sampled(args, local):
     td = float(np.median([e[0].elapsed_time(e[1]) for e in ev]))
     tv = float(np.median([e[1].elapsed_time(e[2]) for e in ev]))
     tau = float((acc[W:].float() + 1).mean().item())
+    # the sampling kernels' own share of a round (their launch-level CUDA-event times)
+    sess.set_profiling(True)
+    for r in range(K + W, K + W + 3):
+        sess.draft_block_sampled(T, ud[r], drafts)
+        sess.verify_sampled(T, drafts, uv[r], acc[0], emit)
+    torch.cuda.synchronize()
+    sess.set_profiling(False)
+    prof = sess.profile()["sampling"]
     sess.close()
     print(json.dumps({
         "metric": "sampled draft+verify round latency (ms) and effective tokens/s, one GB300", "value": b * tau / (td + tv) * 1e3,
         "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": td + tv, "higher_is_better": True,
         "t_draft_ms": td, "t_verify_ms": tv, "tau_measured": tau, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "batch": b, "block": B, "temperature": T,
+        "sampling_kernels": {"ms_per_round": prof["ms"] / 3, "launches_per_round": prof["launches"] / 3,
+                             "gbs": prof["bytes"] / max(prof["ms"], 1e-9) / 1e6},
+        "config": {"workload": w.name, "batch": b, "block": B, "temperature": T, "top_k": args.top_k,
+                   "top_p": args.top_p,
                    "proposals": "the drafter's own, drawn at T; uniforms from a seeded device generator"}}))
 
 
@@ -714,6 +726,8 @@ def main():
                     help="run the rounds at block B below the configured one (dflash_set_block_size)")
     ap.add_argument("--temperature", type=float, default=0.0,
                     help="T > 0: time sampled rounds (speculative rejection sampling) instead of greedy ones")
+    ap.add_argument("--top-k", type=int, default=0, help="with --temperature: top-k filter of both laws (0: off)")
+    ap.add_argument("--top-p", type=float, default=1.0, help="with --temperature: top-p filter of both laws (1: off)")
     ap.add_argument("--train-forward", type=int, default=0, metavar="M",
                     help="time the drafter's training forward with M anchor blocks instead of rounds")
     ap.add_argument("--no-cpu-baseline", action="store_true")

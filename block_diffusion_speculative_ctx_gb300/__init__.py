@@ -8,7 +8,7 @@ calls raise.
 
 The functions carry the C names:
 
-    dflash_init, dflash_prefill, dflash_set_block_size, dflash_block_size,
+    dflash_init, dflash_prefill, dflash_set_block_size, dflash_block_size, dflash_set_sampling_filter,
     dflash_draft_block, dflash_verify,
     dflash_draft_block_sampled, dflash_verify_sampled, dflash_train_forward,
     dflash_generate, dflash_inspect, dflash_destroy, dflash_last_error
@@ -37,7 +37,7 @@ DFLASH_FLAG_KEEP_LOGITS = 1
 DFLASH_FLAG_PROFILE = 2
 DFLASH_FLAG_NO_GRAPHS = 4
 KERNEL_CLASSES = ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "gemm_fc", "gemm_ctx_kv",
-                  "attention", "norm", "rope_store", "swiglu", "argmax", "other")
+                  "attention", "norm", "rope_store", "swiglu", "argmax", "other", "sampling")
 DFLASH_MAX_CTX_LAYERS = 16
 (INSPECT_LENGTHS, INSPECT_ANCHORS, INSPECT_POSTERIOR, INSPECT_TARGET_K, INSPECT_TARGET_V, INSPECT_DRAFT_K,
  INSPECT_DRAFT_V, INSPECT_LOGITS_PREFILL, INSPECT_LOGITS_DRAFT, INSPECT_LOGITS_VERIFY, INSPECT_STATS,
@@ -82,7 +82,7 @@ class dflash_profile_entry(ctypes.Structure):
 
 
 EXPORTS = ("dflash_init", "dflash_prefill", "dflash_set_block_size", "dflash_block_size", "dflash_draft_block", "dflash_verify", "dflash_draft_block_sampled",
-           "dflash_verify_sampled", "dflash_train_forward", "dflash_generate",
+           "dflash_verify_sampled", "dflash_set_sampling_filter", "dflash_train_forward", "dflash_generate",
            "dflash_inspect", "dflash_set_profiling", "dflash_destroy", "dflash_last_error")
 
 _lib = None
@@ -115,13 +115,14 @@ def load(build_if_missing: bool = False):
     lib.dflash_inspect.argtypes = [P, I32, I32, I32, P, SZ, ctypes.POINTER(SZ)]
     lib.dflash_set_profiling.argtypes = [P, I32]
     lib.dflash_set_block_size.argtypes = [P, I32]
+    lib.dflash_set_sampling_filter.argtypes = [P, I32, ctypes.c_float]
     lib.dflash_block_size.argtypes = [P]
     lib.dflash_block_size.restype = I32
     lib.dflash_destroy.argtypes = [P]
     lib.dflash_last_error.argtypes = [P]
     lib.dflash_last_error.restype = ctypes.c_char_p
     for f in ("dflash_init", "dflash_prefill", "dflash_draft_block", "dflash_verify", "dflash_draft_block_sampled",
-              "dflash_verify_sampled", "dflash_train_forward", "dflash_generate",
+              "dflash_verify_sampled", "dflash_set_sampling_filter", "dflash_train_forward", "dflash_generate",
               "dflash_inspect", "dflash_set_profiling", "dflash_set_block_size"):
         getattr(lib, f).restype = ctypes.c_int
     lib.dflash_destroy.restype = None

@@ -94,13 +94,15 @@ struct dflash_ctx {
     // temperature sampling: draft logits kept for verify, softmax row statistics,
     // uniforms and temperatures (device memory, so captured graphs stay valid)
     float* dlogits = nullptr;
-    float2* dstat = nullptr;
-    float2* tstat = nullptr;
+    LawStat* dstat = nullptr;              // filtered draft laws of the last sampled draft
+    LawStat* tstat = nullptr;              // filtered target laws of the last sampled verify
     float* u_draft = nullptr;
     float* u_verify = nullptr;
-    float* temp_dev = nullptr;
-    float* temp_pinned = nullptr;          // host staging of the two temperatures
-    float temp_cur[2] = {-1.f, -1.f};      // values last written to temp_dev
+    SampleParams* prm_dev = nullptr;       // temperatures, top-p, top-k (read by the sampling kernels)
+    SampleParams* prm_pinned = nullptr;    // host staging of prm_dev
+    float temp_cur[2] = {-1.f, -1.f};      // temperatures last written to prm_dev
+    int top_k = 0;                         // filter last written to prm_dev (0 / 1: off)
+    float top_p = 1.f;
     bool draft_sampled = false;
     bool draft_logits_out = false;         // the draft pass also writes its logits to dlogits
     void* feat = nullptr;
@@ -737,8 +739,8 @@ struct Pass {
         head(0, b * B, c->draft_norm, c->drafts, c->keep_draft, B,
              (sampled || c->draft_logits_out) ? c->dlogits : nullptr);
         if (sampled)  // drafts[s][j] = draw from q of row s*B + 1 + j (replaces the argmax)
-            timed(c, DFLASH_K_ARGMAX, (double)b * (B - 1) * c->V * 8, 0, [&] {
-                draft_sample(L, c->dlogits, c->V, b, B, c->temp_dev, c->u_draft, c->dstat, c->drafts);
+            timed(c, DFLASH_K_SAMPLING, (double)b * (B - 1) * c->V * 4, 0, [&] {
+                draft_sample(L, c->dlogits, c->V, b, B, c->prm_dev, c->u_draft, c->dstat, c->drafts);
             });
     }
 
@@ -765,8 +767,8 @@ struct Pass {
             cudaMemcpyAsync(c->keep_hidden, c->x, (size_t)b * B * c->d * 4, cudaMemcpyDeviceToDevice, c->stream);
         head(0, b * B, c->final_norm, c->posterior, c->keep_verify, 0, sampled ? c->logits : nullptr);
         if (sampled) {
-            timed(c, DFLASH_K_ARGMAX, (double)b * B * c->V * 8, 0, [&] {
-                verify_sample(L, c->logits, c->dlogits, c->V, b, B, c->temp_dev, c->proposal, c->u_verify, c->tstat,
+            timed(c, DFLASH_K_SAMPLING, (double)b * (B + 2) * c->V * 4, 0, [&] {
+                verify_sample(L, c->logits, c->dlogits, c->V, b, B, c->prm_dev, c->proposal, c->u_verify, c->tstat,
                               c->dstat, c->n, c->anchor, c->accepted, c->bonus, c->ctx_row_seq, c->ctx_row_pos);
             });
         } else {
@@ -923,8 +925,10 @@ dflash_status set_temperature(dflash_ctx* c, int which, float t) {
     if (!(t > 0.f) || !std::isfinite(t)) return c->fail(DFLASH_E_INVAL, "temperature %g is not a positive finite number", t);
     if (c->temp_cur[which] == t) return DFLASH_OK;
     CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-    c->temp_pinned[which] = t;
-    CUDA_TRY(c, cudaMemcpyAsync(c->temp_dev + which, c->temp_pinned + which, 4, cudaMemcpyHostToDevice, c->stream));
+    float* host = which == 0 ? &c->prm_pinned->t_draft : &c->prm_pinned->t_verify;
+    float* dev = which == 0 ? &c->prm_dev->t_draft : &c->prm_dev->t_verify;
+    *host = t;
+    CUDA_TRY(c, cudaMemcpyAsync(dev, host, 4, cudaMemcpyHostToDevice, c->stream));
     c->temp_cur[which] = t;
     return DFLASH_OK;
 }
@@ -1070,15 +1074,21 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     ALLOC(c->kvout, R * 2 * c->kvd * 4);
     ALLOC(c->logits, (size_t)rb * V * 4);
     ALLOC(c->dlogits, (size_t)rb * V * 4);
-    ALLOC(c->dstat, (size_t)rb * sizeof(float2));
-    ALLOC(c->tstat, (size_t)rb * sizeof(float2));
+    ALLOC(c->dstat, (size_t)rb * sizeof(LawStat));
+    ALLOC(c->tstat, (size_t)rb * sizeof(LawStat));
     ALLOC(c->u_draft, (size_t)rb * 4);
     ALLOC(c->u_verify, (size_t)rb * 4);
-    ALLOC(c->temp_dev, 16);
-    if (cudaMallocHost(&c->temp_pinned, 2 * sizeof(float)) != cudaSuccess) {
-        c->temp_pinned = nullptr;
+    ALLOC(c->prm_dev, sizeof(SampleParams));
+    if (cudaMallocHost(&c->prm_pinned, sizeof(SampleParams)) != cudaSuccess) {
+        c->prm_pinned = nullptr;
         c->fail(DFLASH_E_NOMEM, "pinned host allocation failed");
         return bail(DFLASH_E_NOMEM);
+    }
+    *c->prm_pinned = SampleParams{1.f, 1.f, 1.f, 0};  // no filter
+    if (cudaMemcpyAsync(c->prm_dev, c->prm_pinned, sizeof(SampleParams), cudaMemcpyHostToDevice, c->stream) !=
+        cudaSuccess) {
+        c->fail(DFLASH_E_CUDA, "copy of the sampling settings failed");
+        return bail(DFLASH_E_CUDA);
     }
     ALLOC(c->tokens, R * 4);
     ALLOC(c->row_seq, R * 4);
@@ -1196,6 +1206,21 @@ dflash_status dflash_set_block_size(dflash_ctx* c, int32_t block_size) {
 
 int32_t dflash_block_size(const dflash_ctx* c) { return c ? c->B : -1; }
 
+dflash_status dflash_set_sampling_filter(dflash_ctx* c, int32_t top_k, float top_p) {
+    if (!c) return DFLASH_E_INVAL;
+    if (top_k < 0) return c->fail(DFLASH_E_INVAL, "top_k %d is negative", top_k);
+    if (!(top_p > 0.f && top_p <= 1.f)) return c->fail(DFLASH_E_INVAL, "top_p %g outside (0, 1]", top_p);
+    if (c->state == ST_DRAFTED) return c->fail(DFLASH_E_STATE, "set_sampling_filter between a draft and its verify");
+    if (c->top_k == top_k && c->top_p == top_p) return DFLASH_OK;
+    CUDA_TRY(c, cudaStreamSynchronize(c->stream));  // an earlier copy from the staging buffer is done
+    c->prm_pinned->top_p = top_p;
+    c->prm_pinned->top_k = top_k;
+    CUDA_TRY(c, cudaMemcpyAsync(&c->prm_dev->top_p, &c->prm_pinned->top_p, 8, cudaMemcpyHostToDevice, c->stream));
+    c->top_k = top_k;
+    c->top_p = top_p;
+    return DFLASH_OK;
+}
+
 dflash_status dflash_draft_block(dflash_ctx* c, int32_t* draft_tokens) {
     if (!c) return DFLASH_E_INVAL;
     if (c->state != ST_READY) return c->fail(DFLASH_E_STATE, c->state == ST_EMPTY ? "draft_block before prefill" : "draft_block called twice without verify");
@@ -1237,6 +1262,7 @@ dflash_status dflash_draft_block_sampled(dflash_ctx* c, float temperature, const
     if (!c) return DFLASH_E_INVAL;
     if (c->state != ST_READY) return c->fail(DFLASH_E_STATE, c->state == ST_EMPTY ? "draft_block_sampled before prefill" : "draft_block_sampled called twice without verify");
     if (c->B > 1 && (!draft_tokens || !u_draft)) return c->fail(DFLASH_E_INVAL, "NULL argument");
+    if (!sampling_vocab_ok(c->V)) return c->fail(DFLASH_E_INVAL, "vocabulary %d too large for the sampled round", c->V);
     dflash_status s;
     if ((s = set_temperature(c, 0, temperature))) return s;
     if ((s = load_uniforms(c, c->u_draft, u_draft, (size_t)c->batch * (c->B - 1)))) return s;
@@ -1257,6 +1283,7 @@ dflash_status dflash_verify_sampled(dflash_ctx* c, float temperature, const int3
     if (c->state != ST_DRAFTED || (!c->draft_sampled && c->B > 1))
         return c->fail(DFLASH_E_STATE, "verify_sampled needs a preceding draft_block_sampled");
     if ((!draft_tokens && c->B > 1) || !u_verify || !accepted || !emitted) return c->fail(DFLASH_E_INVAL, "NULL argument");
+    if (!sampling_vocab_ok(c->V)) return c->fail(DFLASH_E_INVAL, "vocabulary %d too large for the sampled round", c->V);
     dflash_status s;
     if ((s = set_temperature(c, 1, temperature))) return s;
     if ((s = load_uniforms(c, c->u_verify, u_verify, (size_t)c->batch * c->B))) return s;
@@ -1526,7 +1553,7 @@ void dflash_destroy(dflash_ctx* c) {
     for (auto& e : c->ctx_ev)
         if (e) cudaEventDestroy(e);
     if (c->side_stream) cudaStreamDestroy(c->side_stream);
-    if (c->temp_pinned) cudaFreeHost(c->temp_pinned);
+    if (c->prm_pinned) cudaFreeHost(c->prm_pinned);
     delete c;
 }
 

@@ -207,17 +207,33 @@ void attention_mma(const Launch& L, const AttnParams& p, int sms);
 bool attention_prefill_tc(const Launch& L, const AttnParams& p);
 
 // ---- temperature sampling (sampling.cu)
-// Draft rows s*B + j (j = 1..B-1) of dlogits [batch*B, V]: dstat[row] = (max, sum exp((l - max)/T)),
-// drafts[s*(B-1) + j-1] = inverse-CDF draw of softmax(l/T) with u_draft[s*(B-1) + j-1];
-// temp[0] = draft T (device memory).
-void draft_sample(const Launch& L, const float* dlogits, int V, int batch, int B, const float* temp,
-                  const float* u_draft, float2* dstat, int* drafts);
-// Target-row statistics (temp[1] = verify T), then per sequence: acceptance of the proposals
-// with min(1, p/q) against u_verify[s*B + j], the residual or bonus draw with u_verify[s*B + B-1],
-// and the round's bookkeeping (as accept()).
+// Sampling settings in device memory (captured passes read them at replay):
+// temperatures of the draft and verify laws, top-p (1: off) and top-k (0: off).
+struct SampleParams {
+    float t_draft, t_verify, top_p;
+    int32_t top_k;
+};
+// A filtered law softmax(l / T) of one logit row: m = max l, s = sum of exp((l - m) / T)
+// over the kept tokens; token z is kept when (rank key of l[z], z) ranks at or above
+// (tkey, tid): key > tkey, or key == tkey and z <= tid.
+struct LawStat {
+    float m, s;
+    uint32_t tkey;
+    int32_t tid;
+};
+// Whether a vocabulary of V tokens fits the law clusters (each CTA stages its chunk).
+bool sampling_vocab_ok(int V);
+// Draft rows s*B + j (j = 1..B-1) of dlogits [batch*B, V]: dstat[row] = the filtered law
+// q_j, drafts[s*(B-1) + j-1] = inverse-CDF draw of q_j with u_draft[s*(B-1) + j-1].
+void draft_sample(const Launch& L, const float* dlogits, int V, int batch, int B, const SampleParams* prm,
+                  const float* u_draft, LawStat* dstat, int* drafts);
+// Target laws tstat[row] of every verify row, then per sequence: acceptance of the
+// proposals with min(1, p/q) against u_verify[s*B + j], the residual or bonus draw with
+// u_verify[s*B + B-1], and the round's bookkeeping (as accept()).
 void verify_sample(const Launch& L, const float* logits, const float* dlogits, int V, int batch, int B,
-                   const float* temp, const int* proposal, const float* u_verify, float2* tstat, const float2* dstat,
-                   int* n, int* anchor, int* accepted, int* bonus, int* ctx_row_seq, int* ctx_row_pos);
+                   const SampleParams* prm, const int* proposal, const float* u_verify, LawStat* tstat,
+                   const LawStat* dstat, int* n, int* anchor, int* accepted, int* bonus, int* ctx_row_seq,
+                   int* ctx_row_pos);
 
 // ---- round bookkeeping
 // Block rows of a draft (proposal == nullptr) or verify pass: token of row

@@ -159,6 +159,10 @@ class Session:
         _check(self.ctx, self.lib.dflash_verify(self.ctx, _ptr(proposal), _ptr(accepted), _ptr(bonus)))
         return accepted, bonus
 
+    def set_sampling_filter(self, top_k: int = 0, top_p: float = 1.0):
+        """Top-k / top-p filter of both laws of the following sampled rounds (0 / 1.0: off)."""
+        _check(self.ctx, self.lib.dflash_set_sampling_filter(self.ctx, int(top_k), float(top_p)))
+
     def draft_block_sampled(self, temperature: float, u_draft, out=None):
         """Proposals [batch, B-1] drawn at temperature T with uniforms u_draft [batch, B-1]."""
         if isinstance(u_draft, np.ndarray):

@@ -76,7 +76,8 @@ enum {
     DFLASH_K_SWIGLU = 10,
     DFLASH_K_ARGMAX = 11,
     DFLASH_K_OTHER = 12,
-    DFLASH_K_COUNT = 13
+    DFLASH_K_SAMPLING = 13,    /* filtered laws, draws and acceptance of the sampled round */
+    DFLASH_K_COUNT = 14
 };
 
 /* One kernel class in the profile: launches, summed device time (CUDA events
@@ -244,17 +245,21 @@ dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* draft_tokens, int32_
  * eq. 6-8 and Algorithm 1 steps 2-3, 7-8 and 10; [digest] Paper vs code
  * "Sampling rule").  The method's random numbers are inputs: every draw is
  * the lowest token z whose cumulative weight exceeds u * total weight, for a
- * caller-supplied uniform u in [0, 1).  Top-p / top-k are not applied.
+ * caller-supplied uniform u in [0, 1).  Every law, the drafter's and the
+ * target's, is filtered by the setting of dflash_set_sampling_filter (off by
+ * default).  The vocabulary must fit the sampling kernels (each of up to 8
+ * CTAs of a row stages its share of the row in shared memory: about 390K
+ * tokens), else E_INVAL.
  *
  * dflash_draft_block_sampled: as dflash_draft_block, then the proposal of
- * mask row j is drawn from q_j = softmax(draft logits_j / T) with
+ * mask row j is drawn from q_j = softmax(draft logits_j / T), filtered, with
  * u_draft[s*(B-1) + j-1]; the laws q are kept for the next verify.
  * u_draft: [batch, B-1] float, host (each in [0, 1), else E_INVAL) or device
  * (clamped to [0, 1)); draft_tokens: [batch, B-1] int32 output, host or device.
  * Errors: as dflash_draft_block, plus E_INVAL (T not positive and finite).
  *
  * dflash_verify_sampled: one causal target pass as dflash_verify; with
- * p_j = softmax(verify logits_j / T), proposal j (block row j+1) is accepted
+ * p_j = softmax(verify logits_j / T), filtered, proposal j (block row j+1) is accepted
  * while u_verify[s*B + j] < min(1, p_j(y)/q_{j+1}(y)); at the first rejection
  * the emitted token is drawn from [p_a - q_{a+1}]_+ (normalised), else from
  * p_{B-1}, with u_verify[s*B + B-1].  Caches keep the anchor and the a_i
@@ -265,6 +270,22 @@ dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* draft_tokens, int32_
  * Errors: E_STATE (no dflash_draft_block_sampled since the last verify),
  * E_INVAL (T, NULL, host token or uniform out of range), E_DEVICE_CHECK
  * (device token outside [0, V): treated as a rejection), E_CUDA. */
+/* Top-k / top-p filter of the sampled round's laws ([digest] Paper vs code
+ * "Sampling rule": they apply to both the draft and the target
+ * distributions).  After the temperature, tokens rank by logit, highest
+ * first, equal logits in increasing id; top-k keeps the first top_k of them
+ * (0: all); top-p then keeps each token whose mass ranked before it, under
+ * the top-k law renormalised, is below top_p (1: all); the kept tokens'
+ * probabilities are renormalised, and eq. 6-8 apply to the filtered laws.
+ * The GPU takes each mass in fp32 and sums them exactly in 2^-32 fixed point
+ * (relative to the row's largest probability), so a token whose preceding
+ * mass is within about 1e-6 of top_p may fall on either side; the kept set
+ * is the same on every run.  Applies from the next
+ * sampled draft on; allowed whenever no draft awaits its verify.
+ * Errors: E_INVAL (ctx NULL, top_k < 0, top_p outside (0, 1]), E_STATE
+ * (between a draft and its verify), E_CUDA. */
+dflash_status dflash_set_sampling_filter(dflash_ctx* ctx, int32_t top_k, float top_p);
+
 dflash_status dflash_draft_block_sampled(dflash_ctx* ctx, float temperature, const float* u_draft,
                                         int32_t* draft_tokens);
 dflash_status dflash_verify_sampled(dflash_ctx* ctx, float temperature, const int32_t* draft_tokens,
