@@ -102,7 +102,8 @@ struct Smem {
     static constexpr int X_BYTES = MT * BK * 2;             // bf16 activation tile (MMA operand)
     static constexpr int XRAW_BYTES = NORM_A ? MT * BK * 4 : 0;  // fp32 residual tile (NORM_A)
     static constexpr int STAGE_BYTES = W_BYTES + X_BYTES + XRAW_BYTES;
-    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr int NW_OFF = STAGES * STAGE_BYTES;           // NORM_A: norm weights of each stage's K slice
+    static constexpr int BAR_OFF = NW_OFF + (NORM_A ? STAGES * BK * 4 : 0);
     static constexpr int NBAR = 2 * STAGES + 1 + (NORM_A ? 2 * STAGES : 0);
     static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16 + 64 * 4 + 128 * 4 + 1024;  // + rstd, partial sums, alignment
 };
@@ -177,8 +178,11 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
             for (int i = 0; i < pre; ++i) {
                 uint8_t* st = smem + i * S::STAGE_BYTES;
                 if (NORM_A) {
-                    mbar_arrive_expect_tx(&xraw[i], S::XRAW_BYTES);
-                    tma_load_2d(st + S::W_BYTES + S::X_BYTES, &tmX, &xraw[i], (kb0 + i) * BK, m0, px);
+                    const int kc = (kb0 + i) * BK;
+                    const uint32_t nwb = (uint32_t)min(BK, a.K - kc) * 4u;
+                    mbar_arrive_expect_tx(&xraw[i], S::XRAW_BYTES + nwb);
+                    tma_load_2d(st + S::W_BYTES + S::X_BYTES, &tmX, &xraw[i], kc, m0, px);
+                    bulk_load(smem + S::NW_OFF + i * BK * 4, a.norm_w + kc, nwb, &xraw[i]);
                 } else {
                     tma_load_2d(st + S::W_BYTES, &tmX, &full[i], (kb0 + i) * BK, m0, px);
                 }
@@ -194,8 +198,10 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
                 mbar_arrive_expect_tx(&full[s], FULL_TX);
                 tma_load_2d(st, &tmW, &full[s], kc, n0, pw);
                 if (NORM_A) {
-                    mbar_arrive_expect_tx(&xraw[s], S::XRAW_BYTES);
+                    const uint32_t nwb = (uint32_t)min(BK, a.K - kc) * 4u;
+                    mbar_arrive_expect_tx(&xraw[s], S::XRAW_BYTES + nwb);
                     tma_load_2d(st + S::W_BYTES + S::X_BYTES, &tmX, &xraw[s], kc, m0, px);
+                    bulk_load(smem + S::NW_OFF + s * BK * 4, a.norm_w + kc, nwb, &xraw[s]);
                 } else {
                     tma_load_2d(st + S::W_BYTES, &tmX, &full[s], kc, m0, px);
                 }
@@ -262,20 +268,21 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
             const int s = i % STAGES;
             uint8_t* st = smem + s * S::STAGE_BYTES;
             const int kc = (kb0 + i) * BK;
-            // the norm weights of this stage load while the raw tile is in flight
             const int c = e & 7;
             const int k = kc + 8 * c;
+            // the raw tile and the stage's norm weights land together (one barrier)
+            if (!mbar_wait(&xraw[s], (i / STAGES) & 1, a.err)) ok = false;
+            const float* nw = reinterpret_cast<const float*>(smem + S::NW_OFF + s * BK * 4) + 8 * c;
             float w8[8];
             if (k + 8 <= a.K) {
-                const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.norm_w + k));
-                const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.norm_w + k + 4));
+                const float4 w0 = reinterpret_cast<const float4*>(nw)[0];
+                const float4 w1 = reinterpret_cast<const float4*>(nw)[1];
                 w8[0] = w0.x; w8[1] = w0.y; w8[2] = w0.z; w8[3] = w0.w;
                 w8[4] = w1.x; w8[5] = w1.y; w8[6] = w1.z; w8[7] = w1.w;
             } else {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) w8[j] = (k + j < a.K) ? a.norm_w[k + j] : 0.f;
+                for (int j = 0; j < 8; ++j) w8[j] = (k + j < a.K) ? nw[j] : 0.f;  // past K: not loaded
             }
-            if (!mbar_wait(&xraw[s], (i / STAGES) & 1, a.err)) ok = false;
             const float* xr = reinterpret_cast<const float*>(st + S::W_BYTES + S::X_BYTES);
             uint8_t* xb = st + S::W_BYTES;
             // 16-byte output chunks: row m, k-chunk c (8 elements); swizzle chunk ^ (m & 7)
@@ -716,6 +723,8 @@ bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W,
     CUtensorMap mw, mx;
     if (!make_map(&mw, W, N, K, K, BN)) return false;
     if (norm_a) {
+        // the norm weights reach shared memory by bulk copies of each stage's K slice
+        if ((reinterpret_cast<uintptr_t>(ep->norm_w) & 15) != 0) return false;
         if (!make_map(&mx, ep->x_f32, a_rows, K, ep->ldx, MT, true)) return false;
     } else if (!make_map(&mx, A, a_rows, K, lda, MT)) {
         return false;
