@@ -62,6 +62,8 @@ struct dflash_ctx {
     size_t esz = 4;  // element size of the storage type
 
     int d, H, Hkv, hd, F, V, Lt, Ld, B, k, qd, kvd, qkv_n, max_seq;
+    void* ctx_wkv = nullptr;     // bf16: [Ld * 2 kvd, d], every draft layer's wk, wv stacked (context K/V in one GEMM)
+    float* ctx_knorm = nullptr;  // [Ld * hd]: the draft layers' k_norm, stacked
     int Bmax = 0;      // configured block size: every round buffer is sized for it
     int append_B = 0;  // block size of the verify whose accepted rows await the context append
     int ctx_slot[64];  // target layer -> index in ctx_layer_ids or -1
@@ -502,7 +504,7 @@ struct Pass {
     // target: causal attention over the target cache, capture of context layers
     // into stage; draft: bidirectional attention over [context ; block].
     void layers(bool target, int rows, const int* row_seq, const int* row_pos, int group_rows, int max_keys,
-                bool capture, double keys_total, int rows_per_seq = 0) {
+                bool capture, double keys_total, int rows_per_seq = 0, const int* stable_len = nullptr) {
         Launch L = c->L();
         const int nl = target ? c->Lt : c->Ld;
         const double R = rows, d = c->d, es = c->esz;
@@ -556,6 +558,7 @@ struct Pass {
             ap.Hkv = c->Hkv;
             ap.hd = c->hd;
             ap.max_keys = max_keys;
+            ap.stable_len = stable_len;
             ap.out = c->att;
             ap.ws = c->attn_ws;
             ap.ws_bytes = ATTN_WS_BYTES;
@@ -601,6 +604,20 @@ struct Pass {
                         false);
             }
         });
+        if (qkv_in_epilogue(rows) && c->ctx_wkv) {
+            // every draft layer's K/V of the context rows in one GEMM over the stacked weights;
+            // the epilogue stores each layer's tiles (k-norm, RoPE) into that layer's cache
+            QkvStoreEpi qe = qkv_epi(0, nullptr, c->ctx_knorm, c->dK, c->dV, ctx_seq, ctx_pos);
+            qe.layers = c->Ld;
+            qe.layer_stride = c->kv.layer_stride;
+            qe.norm_stride = c->hd;
+            normed_gemm(DFLASH_K_GEMM_CTX_KV, rows, c->fcout, c->fc_norm, c->ss_fc, (const T*)c->ctx_wkv,
+                        c->Ld * 2 * c->kvd, c->d, c->kvout, 2 * c->kvd, nullptr, 0, nullptr, &qe, c->xn_ctx);
+            if (layer_done)
+                for (int l = 0; l < c->Ld; ++l)
+                    if (cudaEventRecord(layer_done[l], c->stream) != cudaSuccess) c->launch_failed = true;
+            return;
+        }
         for (int l = 0; l < c->Ld; ++l) {
             const LayerW& w = c->dl[l];
             const T* wkv = elem<T>(w.wqkv, (size_t)c->qd * c->d);  // rows wk, wv
@@ -733,7 +750,8 @@ struct Pass {
         // that the pass is the same launch sequence every round (graph replay)
         double keys = 0;
         for (int s = 0; s < b; ++s) keys += c->n_upper[s] + B;
-        layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, false, keys, B);
+        // (the n committed context entries are complete before each layer's attention starts)
+        layers(false, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, false, keys, B, c->n);
         join_append();  // (already joined by the last layer's attention; kept for clarity)
         // drafts[s][j] = argmax of row s*B + 1 + j
         head(0, b * B, c->draft_norm, c->drafts, c->keep_draft, B,
@@ -762,7 +780,7 @@ struct Pass {
         });
         double keys = 0;
         for (int s = 0; s < b; ++s) keys += c->n_upper[s] + B;
-        layers(true, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, true, keys, B);
+        layers(true, b * B, c->row_seq, c->row_pos, attn_group_rows(B, g), c->max_seq, true, keys, B, c->n);
         if (c->keep_hidden)
             cudaMemcpyAsync(c->keep_hidden, c->x, (size_t)b * B * c->d * 4, cudaMemcpyDeviceToDevice, c->stream);
         head(0, b * B, c->final_norm, c->posterior, c->keep_verify, 0, sampled ? c->logits : nullptr);
@@ -1015,6 +1033,20 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
         if ((s = pack_layer(c, w->target[l], c->tl[l], cfg->target_qk_norm != 0))) return bail(s);
     for (int l = 0; l < c->Ld; ++l)
         if ((s = pack_layer(c, w->draft[l], c->dl[l], true))) return bail(s);
+    if (cfg->dtype == DFLASH_DTYPE_BF16 && c->hd == 128) {
+        // the context K/V of every draft layer comes from the same feature: one stacked GEMM
+        c->ctx_wkv = dev_alloc(c, (size_t)c->Ld * 2 * c->kvd * d * c->esz);
+        c->ctx_knorm = (float*)dev_alloc(c, (size_t)c->Ld * c->hd * 4);
+        if (!c->ctx_wkv || !c->ctx_knorm) return bail(c->fail(DFLASH_E_NOMEM, "weight allocation failed"));
+        for (int l = 0; l < c->Ld; ++l) {
+            if ((s = copy_rows(c, c->ctx_wkv, (size_t)l * 2 * c->kvd, w->draft[l].wk, c->kvd, d))) return bail(s);
+            if ((s = copy_rows(c, c->ctx_wkv, (size_t)l * 2 * c->kvd + c->kvd, w->draft[l].wv, c->kvd, d)))
+                return bail(s);
+            if (cudaMemcpyAsync(c->ctx_knorm + (size_t)l * c->hd, c->dl[l].k_norm, (size_t)c->hd * 4,
+                                cudaMemcpyDeviceToDevice, c->stream) != cudaSuccess)
+                return bail(c->fail(DFLASH_E_CUDA, "copy of the draft k-norms failed"));
+        }
+    }
 
     // caches: identity page mapping, one run of pages per sequence
     c->kv.page_tokens = PAGE_TOKENS;

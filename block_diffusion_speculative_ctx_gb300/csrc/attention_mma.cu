@@ -115,8 +115,6 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 template <int HD>
 __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
-    pdl_wait();
-    pdl_trigger();
     using SM = AttnSmem<HD>;
     constexpr int CH = HD / 8;         // 16-byte chunks per row
     constexpr int NB_O = HD / 8;       // n-blocks of the output
@@ -134,7 +132,8 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
     const int nv = nrows * g;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // sequence of this group: from the row layout when it is sequence-major, else from row_seq
-    const int seq = p.seq_div > 0 ? r0 / p.seq_div : p.row_seq[r0];
+    // (read after the dependency wait)
+    int seq = p.seq_div > 0 ? r0 / p.seq_div : -1;
 
     const uint8_t* Kc = reinterpret_cast<const uint8_t*>(p.Kc);
     const uint8_t* Vc = reinterpret_cast<const uint8_t*>(p.Vc);
@@ -156,10 +155,19 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
         }
         cp_commit();
     };
-    // this rank's first tile (index `rank`, inside the sequence's page range) loads while
-    // the key limits are read; it is dropped below if the sequence is shorter
-    const bool early = seq >= 0 && (int)rank < p.kv.pages_per_seq;
-    if (early) load_tile((int)rank, 0);
+    // this rank's first tile (index `rank`): when it lies inside the sequence's stable keys
+    // it loads before the dependency wait, under the tail of the kernel that writes Q and
+    // the block's K/V; otherwise right after the wait, while the key limits are read (it is
+    // dropped below if the sequence is shorter)
+    bool loaded = false;
+    if (seq >= 0 && p.stable_len && (int)rank < p.kv.pages_per_seq && ((int)rank + 1) * KT <= p.stable_len[seq]) {
+        load_tile((int)rank, 0);
+        loaded = true;
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (p.seq_div <= 0) seq = p.row_seq[r0];
+    if (!loaded && seq >= 0 && (int)rank < p.kv.pages_per_seq) load_tile((int)rank, 0);
 
     if (tid == 0) glim_s = 0;
     __syncthreads();

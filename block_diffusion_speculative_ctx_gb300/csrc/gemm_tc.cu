@@ -63,6 +63,9 @@ struct QkvEpi {
     const int* page_table;
     const int* row_seq;
     const int* row_pos;
+    int layer_tiles;          // tiles of one layer (q_tiles + 2 n_kv)
+    long long layer_stride;   // cache elements between layers
+    int norm_stride;          // k_norm floats between layers
 };
 
 struct TcArgs {
@@ -484,9 +487,11 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
         }
         if (a.epi == 3) {
             const QkvEpi& Q = a.qkv;
-            const int kind = nt < Q.q_tiles ? 0 : (nt < Q.q_tiles + Q.n_kv ? 1 : 2);  // q / k / v head
-            const int head = kind == 0 ? nt : (kind == 1 ? nt - Q.q_tiles : nt - Q.q_tiles - Q.n_kv);
-            const float* nw = kind == 0 ? Q.q_norm : (kind == 1 ? Q.k_norm : nullptr);
+            const int layer = nt / Q.layer_tiles, lt = nt - layer * Q.layer_tiles;
+            const int kind = lt < Q.q_tiles ? 0 : (lt < Q.q_tiles + Q.n_kv ? 1 : 2);  // q / k / v head
+            const int head = kind == 0 ? lt : (kind == 1 ? lt - Q.q_tiles : lt - Q.q_tiles - Q.n_kv);
+            const float* nw =
+                kind == 0 ? Q.q_norm : (kind == 1 && Q.k_norm ? Q.k_norm + (size_t)layer * Q.norm_stride : nullptr);
             if (nw) {
                 // per-head RMSNorm over the tile's 128 rows (each thread rescales only its own row)
                 for (int j = j0; j < j1; ++j) {
@@ -521,7 +526,7 @@ __global__ void __launch_bounds__(THREADS, (MT <= 64 ? 2 : 1)) tc_gemm_kernel(co
                 if (kind == 0) {
                     Q.q_out[(size_t)m * Q.q_tiles * BN + (size_t)head * BN + row] = o;
                 } else {
-                    __nv_bfloat16* base = kind == 1 ? Q.Kc : Q.Vc;
+                    __nv_bfloat16* base = (kind == 1 ? Q.Kc : Q.Vc) + (size_t)layer * Q.layer_stride;
                     base[kv_offset(Q.kv, Q.page_table, seq, pos, head) + row] = o;
                 }
             }
@@ -767,7 +772,11 @@ bool gemm_tc(const Launch& L, const bf16* A, int lda, int a_rows, const bf16* W,
         a.qkv.page_table = src.page_table;
         a.qkv.row_seq = src.row_seq;
         a.qkv.row_pos = src.row_pos;
-        if (N != (src.q_heads + 2 * src.kv_heads) * BN) return false;
+        a.qkv.layer_tiles = src.q_heads + 2 * src.kv_heads;
+        a.qkv.layer_stride = src.layer_stride;
+        a.qkv.norm_stride = src.norm_stride;
+        if (src.layers < 1 || N != src.layers * (src.q_heads + 2 * src.kv_heads) * BN) return false;
+        if (src.layers > 1 && src.q_heads != 0) return false;  // stacked layers: context K/V only
     }
     if (a.ss_out && a.epi != 0) return false;
     if (a.epi == 2 && !a.keys) return false;

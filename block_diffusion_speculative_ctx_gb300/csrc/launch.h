@@ -91,6 +91,12 @@ struct QkvStoreEpi {
     const int* page_table;
     const int* row_seq;    // [M]; < 0 = skip
     const int* row_pos;
+    // Several layers in one GEMM (the drafter's context K/V): N = layers * (q_heads +
+    // 2 * kv_heads) * hd; the tiles of layer l store into Kc / Vc + l * layer_stride
+    // elements with k_norm + l * norm_stride.
+    int layers = 1;
+    long long layer_stride = 0;
+    int norm_stride = 0;
 };
 
 struct GemmEpi {
@@ -193,6 +199,9 @@ struct AttnParams {
                           // row r is r / seq_div (row_seq < 0 still marks an inactive sequence)
     int H, Hkv, hd;
     int max_keys;         // host upper bound on keys seen by any row
+    const int* stable_len = nullptr;  // with seq_div: keys [0, stable_len[s]) of sequence s were written
+                                      // before the launch (earlier passes or joined streams), so their
+                                      // tiles may load before the dependency wait; nullptr: none
     void* out;            // T [rows, H*hd]
     float* ws;            // split workspace (fp32)
     size_t ws_bytes;
