@@ -159,28 +159,37 @@ __global__ void __launch_bounds__(NTHR) attn_mma_kernel(MmaArgs a) {
     // it loads before the dependency wait, under the tail of the kernel that writes Q and
     // the block's K/V; otherwise right after the wait, while the key limits are read (it is
     // dropped below if the sequence is shorter)
+    // key limit of each query vector (causal: its position + 1; else seq_len + extra)
+    auto key_limits = [&]() {
+        if (tid == 0) glim_s = 0;
+        __syncthreads();
+        for (int v = tid; v < QV; v += NTHR) {
+            int lim = 0;
+            if (v < nv && seq >= 0) {
+                const int r = r0 + v / g;
+                if (p.row_seq[r] >= 0) lim = p.seq_len ? (p.seq_len[seq] + p.extra) : (p.row_pos[r] + 1);
+            }
+            lim_s[v] = lim;
+            atomicMax(&glim_s, lim);
+        }
+        __syncthreads();
+    };
     bool loaded = false;
-    if (seq >= 0 && p.stable_len && (int)rank < p.kv.pages_per_seq && ((int)rank + 1) * KT <= p.stable_len[seq]) {
-        load_tile((int)rank, 0);
-        loaded = true;
+    // round passes (stable_len set): the rows' metadata and lengths were written at the start of
+    // the pass or earlier, so the limits are read before the dependency wait too
+    const bool early = p.stable_len != nullptr && p.seq_div > 0;
+    if (early) {
+        if ((int)rank < p.kv.pages_per_seq && ((int)rank + 1) * KT <= p.stable_len[seq]) {
+            load_tile((int)rank, 0);
+            loaded = true;
+        }
+        key_limits();
     }
     pdl_wait();
     pdl_trigger();
     if (p.seq_div <= 0) seq = p.row_seq[r0];
     if (!loaded && seq >= 0 && (int)rank < p.kv.pages_per_seq) load_tile((int)rank, 0);
-
-    if (tid == 0) glim_s = 0;
-    __syncthreads();
-    for (int v = tid; v < QV; v += NTHR) {
-        int lim = 0;
-        if (v < nv && seq >= 0) {
-            const int r = r0 + v / g;
-            if (p.row_seq[r] >= 0) lim = p.seq_len ? (p.seq_len[seq] + p.extra) : (p.row_pos[r] + 1);
-        }
-        lim_s[v] = lim;
-        atomicMax(&glim_s, lim);
-    }
-    __syncthreads();
+    if (!early) key_limits();
     const int glim = glim_s;
     const int tiles = (glim + KT - 1) / KT;
 

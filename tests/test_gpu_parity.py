@@ -172,6 +172,20 @@ def test_small_bf16_stepwise():
     assert run_stepwise("small_bf16", rounds=4) >= 4          # of 2 x 4
 
 
+def test_small_bf16_head_dim_64_stepwise():
+    """bf16 with 64-wide heads (16 query heads, 8 per KV head): the separate q/k norm + RoPE +
+    store kernel, the 64-wide mma.sync attention for prefill and rounds, and the per-layer
+    context K/V GEMMs (the stacked one and the fused epilogues serve 128-wide heads)."""
+    assert run_stepwise("small_bf16", rounds=3, taus=(1, 5, 2), head_dim=64, n_heads=16) >= 3
+
+
+@pytest.mark.parametrize("n_kv", [8, 4, 1])
+def test_small_bf16_gqa_ratios_stepwise(n_kv):
+    """Query heads per KV head of 1, 2 and 8 (the benchmark models use 4): attention query
+    groups of 64 / g vectors per block row, tcgen05 prefill groups of 128 / g rows."""
+    assert run_stepwise("small_bf16", rounds=3, taus=(1, 5, 2), n_kv_heads=n_kv) >= 3
+
+
 def test_small_bf16_prompt_longer_than_a_prefill_chunk():
     assert run_stepwise("small_bf16_long", rounds=3) >= 3     # of 2 x 3
 
