@@ -55,7 +55,7 @@ class dflash_config(ctypes.Structure):
                 ("ctx_layer_ids", ctypes.c_int32 * DFLASH_MAX_CTX_LAYERS), ("mask_token", ctypes.c_int32),
                 ("max_batch", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_double), ("alloc", ALLOC_FN),
-                ("free", FREE_FN), ("alloc_user", ctypes.c_void_p)]
+                ("free", FREE_FN), ("alloc_user", ctypes.c_void_p), ("kv_pool_tokens", ctypes.c_int64)]
 
 
 class dflash_layer_weights(ctypes.Structure):

@@ -79,7 +79,15 @@ struct dflash_ctx {
 
     KVLayout kv;
     void *tK = nullptr, *tV = nullptr, *dK = nullptr, *dV = nullptr;
-    int* page_table = nullptr;
+    int* page_table = nullptr;        // [max_batch * pages_per_seq]: physical page of each (slot, logical page)
+    // KV page pool (host side): physical pages [0, pool_pages) of the caches, the last one a
+    // scratch page that backs every unassigned table entry (never handed out)
+    int pool_pages = 0;
+    std::vector<int> free_pages;      // stack of unassigned pages
+    std::vector<int> slot_pages;      // logical pages assigned to each slot
+    std::vector<int> pt_host;         // mirror of page_table
+    bool pt_full = false;             // the whole table must be uploaded (after a reset)
+    std::vector<int> pt_pending;      // table entries assigned since the last upload
     float2* rope = nullptr;
 
     int R = 0;  // row capacity
@@ -267,6 +275,7 @@ dflash_status validate(const dflash_config* c, std::string& why) {
     if (c->mask_token < 0 || c->mask_token >= c->vocab) return bad("mask_token outside [0, vocab)");
     if (c->max_batch < 1 || c->max_batch > 1024) return bad("max_batch must be in [1, 1024]");
     if (c->max_seq_len < c->block_size + 1) return bad("max_seq_len too small");
+    if (c->kv_pool_tokens < 0 || c->kv_pool_tokens > (1ll << 36)) return bad("kv_pool_tokens must be in [0, 2^36]");
     if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.0)) return bad("rms_eps and rope_theta must be positive");
     if ((c->alloc == nullptr) != (c->free == nullptr)) return bad("alloc and free must both be set or both NULL");
     if ((double)c->max_batch * c->block_size * 2 * c->ffn > 2e9) return bad("batch x block x ffn too large");
@@ -800,6 +809,64 @@ struct Pass {
     }
 };
 
+// ---- KV page pool
+// Every slot's table row returns to the scratch page and every page to the pool.
+void pool_reset(dflash_ctx* c) {
+    const int scratch = c->pool_pages - 1;
+    c->free_pages.clear();
+    for (int p = scratch - 1; p >= 0; --p) c->free_pages.push_back(p);
+    c->slot_pages.assign(c->cfg.max_batch, 0);
+    c->pt_host.assign((size_t)c->cfg.max_batch * c->kv.pages_per_seq, scratch);
+    c->pt_full = true;
+    c->pt_pending.clear();
+}
+
+// Back positions [0, tokens) of `slot` with pages; false when the pool runs out.
+bool pool_ensure(dflash_ctx* c, int slot, long long tokens) {
+    const int pps = c->kv.pages_per_seq;
+    const long long need_ll = (tokens + PAGE_TOKENS - 1) / PAGE_TOKENS;
+    const int need = (int)std::min<long long>(need_ll, pps);
+    while (c->slot_pages[slot] < need) {
+        if (c->free_pages.empty()) return false;
+        const size_t e = (size_t)slot * pps + c->slot_pages[slot]++;
+        c->pt_host[e] = c->free_pages.back();
+        c->free_pages.pop_back();
+        c->pt_pending.push_back((int)e);
+    }
+    return true;
+}
+
+// The device page table follows the host mirror, in stream order: after a reset the whole table
+// (a pageable copy, which may wait for the stream: prefill, init and the training forward only);
+// between rounds the few new entries, written by a kernel that carries them in its parameters,
+// so that the rounds stay asynchronous.
+dflash_status pool_upload(dflash_ctx* c) {
+    if (c->pt_full) {
+        CUDA_TRY(c, cudaMemcpyAsync(c->page_table, c->pt_host.data(), c->pt_host.size() * 4,
+                                    cudaMemcpyHostToDevice, c->stream));
+        c->pt_full = false;
+        c->pt_pending.clear();
+        return DFLASH_OK;
+    }
+    Launch L = c->L();
+    for (size_t i = 0; i < c->pt_pending.size(); i += 64) {
+        PageUpdates u;
+        u.n = (int)std::min<size_t>(64, c->pt_pending.size() - i);
+        for (int j = 0; j < u.n; ++j) {
+            u.idx[j] = c->pt_pending[i + j];
+            u.page[j] = c->pt_host[c->pt_pending[i + j]];
+        }
+        set_pages(L, c->page_table, u);
+    }
+    c->pt_pending.clear();
+    return launch_check(c);
+}
+
+dflash_status pool_full(dflash_ctx* c, int slot, long long tokens) {
+    return c->fail(DFLASH_E_CAPACITY, "KV page pool exhausted: sequence %d needs %lld tokens (%d pages of %d in use)",
+                   slot, tokens, c->pool_pages - 1 - (int)c->free_pages.size(), c->pool_pages - 1);
+}
+
 dflash_status capacity_check(dflash_ctx* c) {
     for (int s = 0; s < c->batch; ++s) {
         if (c->n_upper[s] + c->B > c->cfg.max_seq_len) {
@@ -813,7 +880,16 @@ dflash_status capacity_check(dflash_ctx* c) {
                                c->n_upper[s], c->B, c->cfg.max_seq_len);
         }
     }
-    return DFLASH_OK;
+    // pages for every position the round may write (the block at n .. n+B-1)
+    for (int s = 0; s < c->batch; ++s)
+        if (!pool_ensure(c, s, (long long)c->n_upper[s] + c->B)) {
+            std::vector<int> nh(c->batch);  // the bound may be loose: refresh it from the device first
+            CUDA_TRY(c, cudaMemcpyAsync(nh.data(), c->n, (size_t)c->batch * 4, cudaMemcpyDeviceToHost, c->stream));
+            CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+            c->n_upper = nh;
+            if (!pool_ensure(c, s, (long long)c->n_upper[s] + c->B)) return pool_full(c, s, (long long)c->n_upper[s] + c->B);
+        }
+    return pool_upload(c);
 }
 
 dflash_status launch_check(dflash_ctx* c) {
@@ -1054,21 +1130,20 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     c->kv.pages_per_seq = c->max_seq / PAGE_TOKENS;
     c->kv.n_kv_heads = c->Hkv;
     c->kv.head_dim = c->hd;
-    const size_t pages = (size_t)cfg->max_batch * c->kv.pages_per_seq;
-    c->kv.layer_stride = (long long)(pages * c->Hkv * PAGE_TOKENS * c->hd);
+    const size_t table = (size_t)cfg->max_batch * c->kv.pages_per_seq;
+    const long long pool_tokens =
+        cfg->kv_pool_tokens > 0 ? cfg->kv_pool_tokens : (long long)cfg->max_batch * c->max_seq;
+    c->pool_pages = (int)((pool_tokens + PAGE_TOKENS - 1) / PAGE_TOKENS) + 1;  // + the scratch page
+    c->kv.layer_stride = (long long)c->pool_pages * c->Hkv * PAGE_TOKENS * c->hd;
     ALLOC(c->tK, (size_t)c->Lt * c->kv.layer_stride * esz);
     ALLOC(c->tV, (size_t)c->Lt * c->kv.layer_stride * esz);
     ALLOC(c->dK, (size_t)c->Ld * c->kv.layer_stride * esz);
     ALLOC(c->dV, (size_t)c->Ld * c->kv.layer_stride * esz);
-    ALLOC(c->page_table, pages * 4);
-    {
-        std::vector<int> pt(pages);
-        for (size_t i = 0; i < pages; ++i) pt[i] = (int)i;
-        if (cudaMemcpyAsync(c->page_table, pt.data(), pages * 4, cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
-            cudaStreamSynchronize(c->stream) != cudaSuccess) {
-            c->fail(DFLASH_E_CUDA, "page table upload failed");
-            return bail(DFLASH_E_CUDA);
-        }
+    ALLOC(c->page_table, table * 4);
+    pool_reset(c);
+    if (pool_upload(c) != DFLASH_OK || cudaStreamSynchronize(c->stream) != cudaSuccess) {
+        c->fail(DFLASH_E_CUDA, "page table upload failed");
+        return bail(DFLASH_E_CUDA);
     }
     // RoPE table: angle pos * theta^(-2j/hd) in double, stored as fp32 (cos, sin)
     ALLOC(c->rope, (size_t)c->max_seq * (c->hd / 2) * sizeof(float2));
@@ -1208,6 +1283,21 @@ dflash_status dflash_prefill(dflash_ctx* c, int32_t batch, const int32_t* lens, 
     }
     for (size_t i = 0; i < total; ++i)
         if (toks[i] < 0 || toks[i] >= c->V) return c->fail(DFLASH_E_INVAL, "prompt token %zu = %d outside [0, %d)", i, toks[i], c->V);
+    // a new batch: every page returns to the pool, then each prompt (+ one block) takes its own
+    pool_reset(c);
+    for (int s = 0; s < batch; ++s)
+        if (!pool_ensure(c, s, (long long)lens[s] + c->B)) {
+            const dflash_status st = pool_full(c, s, (long long)lens[s] + c->B);
+            pool_reset(c);
+            c->batch = 0;
+            c->state = ST_EMPTY;
+            const dflash_status up = pool_upload(c);
+            return up ? up : st;
+        }
+    {
+        dflash_status st = pool_upload(c);
+        if (st) return st;
+    }
     c->batch = batch;
     c->state = ST_EMPTY;
     c->pending_append = false;
@@ -1350,21 +1440,31 @@ dflash_status dflash_train_forward(dflash_ctx* c, int32_t n_tokens, const int32_
     int first = 0;
     dflash_status s = dflash_prefill(c, 1, &n_tokens, tokens, &first);
     if (s) return s;
-    // 2. slot i+1 shares slot 0's pages below its anchor's page and owns the rest
+    // 2. slot i+1 shares slot 0's pages below its anchor's page and takes its own pages from the
+    //    pool for the rest of its block
     const int pps = c->kv.pages_per_seq;
-    const size_t pages = (size_t)c->cfg.max_batch * pps;
-    std::vector<int> pt(pages), ident(pages);
-    for (size_t i = 0; i < pages; ++i) pt[i] = ident[i] = (int)i;
-    for (int i = 0; i < m; ++i)
-        for (int t = 0; t < (anchors[i] >> PAGE_SHIFT); ++t) pt[(size_t)(i + 1) * pps + t] = t;
-    CUDA_TRY(c, cudaMemcpyAsync(c->page_table, pt.data(), pages * 4, cudaMemcpyHostToDevice, c->stream));
+    for (int i = 0; i < m; ++i) {
+        const int p0 = anchors[i] >> PAGE_SHIFT;
+        for (int t = 0; t < p0; ++t) c->pt_host[(size_t)(i + 1) * pps + t] = c->pt_host[t];
+        c->slot_pages[i + 1] = p0;
+        if (!pool_ensure(c, i + 1, (long long)anchors[i] + B)) {
+            const dflash_status st = pool_full(c, i + 1, (long long)anchors[i] + B);
+            pool_reset(c);
+            c->batch = 0;
+            c->state = ST_EMPTY;
+            const dflash_status up = pool_upload(c);
+            return up ? up : st;
+        }
+    }
+    if ((s = pool_upload(c))) return s;
     // 3. its own copy of the anchor's page (the context rows below the anchor in that page)
     const size_t page_elems = (size_t)c->Hkv * PAGE_TOKENS * c->hd;
     for (int l = 0; l < c->Ld; ++l)
         for (int i = 0; i < m; ++i) {
             const int p0 = anchors[i] >> PAGE_SHIFT;
-            const size_t src = (size_t)l * c->kv.layer_stride + (size_t)p0 * page_elems;
-            const size_t dst = (size_t)l * c->kv.layer_stride + ((size_t)(i + 1) * pps + p0) * page_elems;
+            const size_t src = (size_t)l * c->kv.layer_stride + (size_t)c->pt_host[p0] * page_elems;
+            const size_t dst =
+                (size_t)l * c->kv.layer_stride + (size_t)c->pt_host[(size_t)(i + 1) * pps + p0] * page_elems;
             CUDA_TRY(c, cudaMemcpyAsync((char*)c->dK + dst * c->esz, (char*)c->dK + src * c->esz, page_elems * c->esz,
                                         cudaMemcpyDeviceToDevice, c->stream));
             CUDA_TRY(c, cudaMemcpyAsync((char*)c->dV + dst * c->esz, (char*)c->dV + src * c->esz, page_elems * c->esz,
@@ -1396,8 +1496,9 @@ dflash_status dflash_train_forward(dflash_ctx* c, int32_t n_tokens, const int32_
     }
     std::vector<float> nll((size_t)m * (B - 1));
     CUDA_TRY(c, cudaMemcpyAsync(nll.data(), c->u_draft, nll.size() * 4, cudaMemcpyDeviceToHost, c->stream));
-    // 7. identity pages again; the session needs a new prefill before any round
-    CUDA_TRY(c, cudaMemcpyAsync(c->page_table, ident.data(), pages * 4, cudaMemcpyHostToDevice, c->stream));
+    // 7. every page back to the pool; the session needs a new prefill before any round
+    pool_reset(c);
+    if ((s = pool_upload(c))) return s;
     CUDA_TRY(c, cudaStreamSynchronize(c->stream));
     c->batch = 0;
     c->state = ST_EMPTY;

@@ -346,4 +346,17 @@ DFL_INST(float)
 DFL_INST(bf16)
 #undef DFL_INST
 
+// KV page table entries assigned by the host pool; the updates travel in the kernel's
+// parameters, so no host buffer outlives the call.
+__global__ void set_pages_kernel(int* __restrict__ table, PageUpdates u) {
+    pdl_wait();
+    pdl_trigger();
+    if ((int)threadIdx.x < u.n) table[u.idx[threadIdx.x]] = u.page[threadIdx.x];
+}
+
+void set_pages(const Launch& L, int* table, const PageUpdates& u) {
+    if (u.n <= 0) return;
+    launch_k(L, set_pages_kernel, dim3(1), dim3(64), 0, 1, table, u);
+}
+
 }  // namespace dfl

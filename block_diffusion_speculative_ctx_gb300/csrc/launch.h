@@ -244,6 +244,14 @@ void verify_sample(const Launch& L, const float* logits, const float* dlogits, i
                    const LawStat* dstat, int* n, int* anchor, int* accepted, int* bonus, int* ctx_row_seq,
                    int* ctx_row_pos);
 
+// ---- KV page table updates during the rounds (kernels.cu): table[idx[i]] = page[i], i < n
+struct PageUpdates {
+    int n;
+    int idx[64];
+    int page[64];
+};
+void set_pages(const Launch& L, int* table, const PageUpdates& u);
+
 // ---- round bookkeeping
 // Block rows of a draft (proposal == nullptr) or verify pass: token of row
 // s*B+j is anchor[s] (j == 0), the mask id (draft) or proposal[s*(B-1)+j-1]

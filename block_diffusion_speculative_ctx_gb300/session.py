@@ -102,7 +102,7 @@ class Session:
 
     def __init__(self, w, max_batch: Optional[int] = None, max_seq_len: Optional[int] = None,
                  keep_logits: bool = False, use_torch_alloc: bool = True, tensors: Optional[dict] = None,
-                 graphs: bool = True):
+                 graphs: bool = True, kv_pool_tokens: int = 0):
         import torch
         if not torch.cuda.is_available():
             raise RuntimeError("no CUDA device: the dflash library has no CPU path")
@@ -114,6 +114,7 @@ class Session:
         self.cfg = config_from_workload(w, self.max_batch, self.max_seq_len, keep_logits)
         if not graphs:
             self.cfg.flags |= DFLASH_FLAG_NO_GRAPHS
+        self.cfg.kv_pool_tokens = int(kv_pool_tokens)  # 0: max_batch * max_seq_len
         self.alloc = _TorchAllocator() if use_torch_alloc else None
         if self.alloc:
             self.cfg.alloc, self.cfg.free = self.alloc.alloc_cb, self.alloc.free_cb

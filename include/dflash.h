@@ -47,7 +47,7 @@ typedef enum {
     DFLASH_E_NOMEM = 2,        /* a device allocation failed */
     DFLASH_E_CUDA = 3,         /* a CUDA runtime call failed */
     DFLASH_E_STATE = 4,        /* call out of order (verify before draft, draft before prefill, ...) */
-    DFLASH_E_CAPACITY = 5,     /* a sequence would grow past max_seq_len */
+    DFLASH_E_CAPACITY = 5,     /* a sequence would grow past max_seq_len, or the KV page pool is full */
     DFLASH_E_TIMEOUT = 6,      /* a bounded device-side wait ran out */
     DFLASH_E_DEVICE_CHECK = 7  /* a device-side argument check failed */
 } dflash_status;
@@ -113,13 +113,15 @@ typedef struct {
     int32_t ctx_layer_ids[DFLASH_MAX_CTX_LAYERS]; /* 0-based target layers, residual after the layer */
     int32_t mask_token;        /* id embedded at the B-1 mask positions */
     int32_t max_batch;         /* sequences per session */
-    int32_t max_seq_len;       /* capacity per sequence: prompt + generated + B */
+    int32_t max_seq_len;       /* longest sequence: prompt + generated + B */
     int32_t flags;             /* DFLASH_FLAG_* */
     float rms_eps;             /* RMSNorm epsilon */
     double rope_theta;         /* RoPE base */
     dflash_alloc_fn alloc;     /* optional allocator (see above) */
     dflash_free_fn free;
     void* alloc_user;
+    int64_t kv_pool_tokens;    /* KV cache capacity shared by the batch, in tokens (rounded up to
+                                  64-token pages); 0 = max_batch * max_seq_len */
 } dflash_config;
 
 /* One decoder layer, device pointers.  wq, wk, wv, w_gate and w_up are read
@@ -170,10 +172,13 @@ typedef struct {
 
 typedef struct dflash_ctx dflash_ctx; /* opaque; owned by the library */
 
-/* Create a session: validate cfg, allocate the paged target KV cache, the
- * draft context cache and all round buffers for max_batch x max_seq_len
- * (nothing is allocated later), and pack the q/k/v and gate/up matrices into
- * the library's layout.  Those packed copies are the session's only weight
+/* Create a session: validate cfg, allocate the paged target KV cache and the
+ * draft context cache (one pool of kv_pool_tokens / 64 pages of 64 tokens,
+ * shared by the batch: a sequence takes pages from the pool as it grows, so
+ * a ragged batch needs only the sum of its lengths, and every page returns to
+ * the pool at the next prefill), all round buffers for max_batch sequences of
+ * up to max_seq_len tokens (nothing is allocated later), and pack the q/k/v
+ * and gate/up matrices into the library's layout.  Those packed copies are the session's only weight
  * memory: (H + 2 H_kv) hd d + 2 F d elements per layer, about 13 of the 19.7 GB
  * of a Qwen3-8B-shaped target with its 5-layer drafter; the caller's wq, wk, wv,
  * w_gate and w_up may be freed once this returns, and every other matrix is
@@ -192,7 +197,8 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
  * prompt_lens: host [batch]; prompt_tokens: host, concatenated (sum of lens);
  * first_tokens: host [batch] output.
  * Errors: E_INVAL (batch outside [1, max_batch], a length < 1, a token outside
- * [0, V)), E_CAPACITY (length + block_size > max_seq_len), E_CUDA. */
+ * [0, V)), E_CAPACITY (length + block_size > max_seq_len, or the KV page pool
+ * cannot hold every prompt + block_size), E_CUDA. */
 dflash_status dflash_prefill(dflash_ctx* ctx, int32_t batch, const int32_t* prompt_lens,
                              const int32_t* prompt_tokens, int32_t* first_tokens);
 

@@ -55,9 +55,10 @@ def test_struct_layouts_match_the_header(tmp_path):
 #include <stddef.h>
 #include "dflash.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(dflash_config), sizeof(dflash_layer_weights),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(dflash_config), sizeof(dflash_layer_weights),
          sizeof(dflash_weights), sizeof(dflash_stats), offsetof(dflash_config, rope_theta),
-         offsetof(dflash_config, alloc_user), offsetof(dflash_weights, draft_norm));
+         offsetof(dflash_config, alloc_user), offsetof(dflash_weights, draft_norm),
+         offsetof(dflash_config, kv_pool_tokens));
   return 0;
 }
 """)
@@ -67,7 +68,7 @@ int main(void) {
     want = [ctypes.sizeof(dfl.dflash_config), ctypes.sizeof(dfl.dflash_layer_weights),
             ctypes.sizeof(dfl.dflash_weights), ctypes.sizeof(dfl.dflash_stats),
             dfl.dflash_config.rope_theta.offset, dfl.dflash_config.alloc_user.offset,
-            dfl.dflash_weights.draft_norm.offset]
+            dfl.dflash_weights.draft_norm.offset, dfl.dflash_config.kv_pool_tokens.offset]
     assert got == want
 
 

@@ -66,7 +66,7 @@ def _rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), schedule=None, **wkw):
+def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), schedule=None, session_kw=None, **wkw):
     """Prefill + `rounds` rounds on both sides; returns the number of
     (sequence, round) pairs compared.  `schedule`: block size of round r =
     schedule[r % len] (dflash_set_block_size on the GPU, the oracle's
@@ -89,7 +89,8 @@ def run_stepwise(name, rounds=6, taus=(1, 4, 7, 16, 3, 2), schedule=None, **wkw)
     streams = [_greedy_stream(m, st, n_ar) for st in states]
     props = [spec.planted_proposer(s, taus, w.vocab) for s in streams]
     alive = [True] * len(states)
-    sess = _session(w, keep_logits=True, max_seq_len=max(w.prompt_lens) + (rounds + 2) * w.block_size + 8)
+    sess = _session(w, keep_logits=True, max_seq_len=max(w.prompt_lens) + (rounds + 2) * w.block_size + 8,
+                    **(session_kw or {}))
     try:
         first = sess.prefill(prompts)
         plog = sess.logits("prefill")
@@ -184,6 +185,35 @@ def test_small_bf16_gqa_ratios_stepwise(n_kv):
     """Query heads per KV head of 1, 2 and 8 (the benchmark models use 4): attention query
     groups of 64 / g vectors per block row, tcgen05 prefill groups of 128 / g rows."""
     assert run_stepwise("small_bf16", rounds=3, taus=(1, 5, 2), n_kv_heads=n_kv) >= 3
+
+
+def test_small_bf16_llama_ragged_batch_in_a_small_page_pool():
+    """Prompts of 64, 5, 130 and 33 tokens in a KV pool of 13 pages, where one run of
+    max_seq_len per sequence would take 20: pages are handed out as the sequences grow, so
+    each sequence's cache is scattered over the pool (prefill, decode attention, the q/k/v
+    store epilogues and the stacked context K/V all follow the page table)."""
+    assert run_stepwise("small_bf16_llama", rounds=6, session_kw={"kv_pool_tokens": 13 * 64}) >= 12
+
+
+def test_page_pool_capacity_errors():
+    from block_diffusion_speculative_ctx_gb300 import DFlashError
+    w = configs.get("tiny_f32_b3")          # prompts of 32, 7 and 19 tokens
+    prompts = synth.prompts(w)
+    B = w.block_size
+    with _session(w, max_seq_len=256, kv_pool_tokens=2 * 64) as sess:
+        with pytest.raises(DFlashError, match="page pool"):
+            sess.prefill(prompts)           # three prompts need three pages
+    with _session(w, max_seq_len=256, kv_pool_tokens=3 * 64) as sess:
+        sess.prefill(prompts)
+        wrong = np.zeros((3, B - 1), np.int32)
+        with pytest.raises(DFlashError, match="page pool"):
+            for _ in range(64):             # one token per round: the 32-token prompt needs a 4th page
+                d = sess.draft_block()
+                wrong[:] = (d + 1) % w.vocab
+                sess.verify(wrong)
+        first = sess.prefill(prompts)       # a new batch returns every page to the pool
+        m = om.Model(w)
+        assert [int(t) for t in first] == [spec.prefill(m, p).anchor for p in prompts]
 
 
 def test_small_bf16_prompt_longer_than_a_prefill_chunk():
