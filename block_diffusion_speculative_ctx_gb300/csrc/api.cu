@@ -1124,7 +1124,8 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
         }
     }
 
-    // caches: identity page mapping, one run of pages per sequence
+    // caches: one pool of 64-token pages shared by the batch (plus a scratch page), assigned per
+    // sequence by the host as it grows; the page table starts with every entry on the scratch page
     c->kv.page_tokens = PAGE_TOKENS;
     c->kv.page_shift = PAGE_SHIFT;
     c->kv.pages_per_seq = c->max_seq / PAGE_TOKENS;
