@@ -75,14 +75,11 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 struct KVLayout {
     int page_tokens;      // tokens per page (power of two)
     int page_shift;       // log2(page_tokens)
-    int pages_per_seq;    // row length of the page table (logical pages of the longest sequence)
+    int pages_per_seq;
     int n_kv_heads;
     int head_dim;
-    long long layer_stride;  // elements per layer of one cache (K or V): the whole page pool
+    long long layer_stride;  // elements per layer of one cache (K or V)
 };
-
-// Element offset of (sequence, position, KV head) in one layer of a cache: the page table maps
-// the sequence's logical page to a physical page of the pool.
 
 __device__ __forceinline__ long long kv_offset(const KVLayout& L, const int* page_table, int seq, int pos,
                                                int kvh) {
