@@ -6,9 +6,13 @@
 // contraction (the round's blocks of 16 rows use attention_mma.cu).
 //
 // A CTA owns 128 query vectors: 128 / g positions of one sequence times the g
-// query heads of one KV head.  Thread t of the 4 warps is query vector t and
-// TMEM lane t.  The CTA walks the 64-key tiles (= cache pages) 0 .. ceil(max
-// position / 64) in order, with a software pipeline per tile t:
+// query heads of one KV head.  Query vector v is TMEM lane v; two threads share
+// it, v (warps 0-3) and v + 128 (warps 4-7, the same TMEM lane quadrants): the
+// first takes key columns 0-31 of each tile and O columns 0-63, the second key
+// columns 32-63 and O columns 64-127, and the two exchange their tile maxima
+// through shared memory (a named barrier per warp pair).  The CTA walks the
+// 64-key tiles (= cache pages) 0 .. ceil(max position / 64) in order, with a
+// software pipeline per tile t:
 //   - S_{t+1} = Q K_{t+1}^T is issued on the tensor cores before the softmax of
 //     tile t runs (S is double-buffered in TMEM: 2 x 64 columns);
 //   - the softmax of tile t is online (fp32, base 2) with a lazy reference max
@@ -37,7 +41,8 @@ using namespace tc;
 constexpr int KT = 64;       // keys per tile = cache page
 constexpr int HD = 128;      // head dim
 constexpr int QM = 128;      // query vectors per CTA (MMA M)
-constexpr int NT = 128;      // threads: 4 warps = the 4 TMEM lane quadrants
+constexpr int NT = 256;      // threads: 8 warps, two per TMEM lane quadrant
+constexpr int KH = KT / 2;   // key columns per thread of a tile
 constexpr int RING = 4;      // K/V ring stages
 
 constexpr int Q_REG = QM * 128;       // 16 KB: one 64-dim half of the 128 query rows
@@ -77,6 +82,7 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
     uint64_t* bar_o = bar_s + 2;                                  // P.V complete
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 3);
     __shared__ int glim_s;
+    __shared__ float xch_s[2][QM];  // the two halves of each query vector: tile max, final sum
 
     const AttnParams& p = a.p;
     const int grp = gridDim.x - 1 - blockIdx.x;  // later positions (more key tiles) first
@@ -86,6 +92,7 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
     const int nrows = min(p.group_rows, p.rows - r0);
     const int nv = nrows * g;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int v = tid & (QM - 1), half = tid >> 7;  // query vector (TMEM lane) and key / O half
     const int seq = p.seq_div > 0 ? r0 / p.seq_div : p.row_seq[r0];
 
     if (warp == 0) {
@@ -103,28 +110,28 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_lane = (uint32_t)(32 * warp) << 16;
-    const uint32_t tO = tmem + t_lane + 128;  // O: columns 128 .. 255
+    const uint32_t t_lane = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t tO = tmem + t_lane + 128 + 64 * half;  // this thread's O columns (of 128 .. 255)
 
     // causal key limit of this thread's query vector
     int lim = 0;
-    if (tid < nv && seq >= 0) {
-        const int r = r0 + tid / g;
+    if (v < nv && seq >= 0) {
+        const int r = r0 + v / g;
         if (p.row_seq[r] >= 0) lim = p.row_pos[r] + 1;
     }
     atomicMax(&glim_s, lim);
-    // Q into the swizzled A operand (padding rows zero)
+    // Q into the swizzled A operand (padding rows zero): each half copies one 64-dim region
     {
         const uint4* src = nullptr;
-        if (tid < nv) {
-            const int r = r0 + tid / g, h = kvh * g + tid % g;
+        if (v < nv) {
+            const int r = r0 + v / g, h = kvh * g + v % g;
             src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + (size_t)r * p.H * HD +
-                                                 (size_t)h * HD);
+                                                 (size_t)h * HD) + 8 * half;
         }
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
+        for (int ch = 0; ch < 8; ++ch) {
             const uint4 x = src ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sm + Q_OFF + (ch >> 3) * Q_REG + swz(tid, ch & 7)) = x;
+            *reinterpret_cast<uint4*>(sm + Q_OFF + half * Q_REG + swz(v, ch)) = x;
         }
     }
     __syncthreads();
@@ -194,38 +201,38 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
         // (B) this tile's scores
         wait(&bar_s[it & 1], (uint32_t)((it >> 1) & 1));
         fence_after();
-        float sc[KT];
+        float sc[KH];
         {
-            const uint32_t tS = tmem + t_lane + (uint32_t)((it & 1) * KT);
-            uint32_t r0_[16], r1_[16], r2_[16], r3_[16];
+            const uint32_t tS = tmem + t_lane + (uint32_t)((it & 1) * KT + KH * half);
+            uint32_t r0_[16], r1_[16];
             tmem_ld16_issue(tS, r0_);
             tmem_ld16_issue(tS + 16, r1_);
-            tmem_ld16_issue(tS + 32, r2_);
-            tmem_ld16_issue(tS + 48, r3_);
             tmem_ld_wait(r0_);
             tmem_ld_wait(r1_);
-            tmem_ld_wait(r2_);
-            tmem_ld_wait(r3_);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 sc[c] = __uint_as_float(r0_[c]);
                 sc[16 + c] = __uint_as_float(r1_[c]);
-                sc[32 + c] = __uint_as_float(r2_[c]);
-                sc[48 + c] = __uint_as_float(r3_[c]);
             }
         }
-        // (C) online softmax, lazy reference max (moves only by more than 2^8)
+        // (C) online softmax, lazy reference max (moves only by more than 2^8); the row's
+        // tile max from both halves (warps w and w + 4 meet at named barrier 1 + w % 4)
         float mx = -INFINITY;
+        const int k0 = it * KT + KH * half;
 #pragma unroll
-        for (int c = 0; c < KT; ++c) {
-            sc[c] = (it * KT + c < lim) ? sc[c] * a.scale_log2 : -INFINITY;
+        for (int c = 0; c < KH; ++c) {
+            sc[c] = (k0 + c < lim) ? sc[c] * a.scale_log2 : -INFINITY;
             mx = fmaxf(mx, sc[c]);
         }
+        xch_s[half][v] = mx;
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+        mx = fmaxf(mx, xch_s[half ^ 1][v]);
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");  // both read before the next write
         const float m_new = (mx > m_run + 8.f) ? mx : m_run;
         const float alpha = (m_new == m_run) ? 1.f : ((m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new));
-        float sum = 0.f;
+        float sum = 0.f;  // this half's share; the halves' running sums are added at the end
 #pragma unroll
-        for (int c = 0; c < KT; ++c) {
+        for (int c = 0; c < KH; ++c) {
             sc[c] = (sc[c] == -INFINITY) ? 0.f : exp2f(sc[c] - m_new);
             sum += sc[c];
         }
@@ -237,7 +244,7 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
             fence_after();
         }
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int ch = 0; ch < 4; ++ch) {  // 16-byte chunks 4 half .. 4 half + 3 of row v
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -245,13 +252,14 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
                 hi[e] = pack2_bf16(x0, x1);
                 lo[e] = pack2_bf16(x0 - __uint_as_float(hi[e] << 16), x1 - __uint_as_float(hi[e] & 0xFFFF0000u));
             }
-            *reinterpret_cast<uint4*>(sm + P_OFF + swz(tid, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(sm + P_OFF + QM * 128 + swz(tid, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4*>(sm + P_OFF + swz(v, 4 * half + ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(sm + P_OFF + QM * 128 + swz(v, 4 * half + ch)) =
+                make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         // rescale the running O when the reference max moved (warp-collective TMEM access)
         if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-            for (int c = 0; c < HD; c += 16) {
+            for (int c = 0; c < HD / 2; c += 16) {
                 float o[16];
                 tmem_ld16(tO + c, o);
 #pragma unroll
@@ -284,15 +292,17 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
         wait(bar_o, (uint32_t)((n - 1) & 1));
         fence_after();
     }
+    xch_s[half][v] = l_run;
     __syncthreads();
     if (n > 0) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        const bool live = okw && tid < nv && lim > 0;
+        const float l = xch_s[0][v] + xch_s[1][v];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool live = okw && v < nv && lim > 0;
         __nv_bfloat16* dst =
-            live ? out + (size_t)(r0 + tid / g) * p.H * HD + (size_t)(kvh * g + tid % g) * HD : nullptr;
+            live ? out + (size_t)(r0 + v / g) * p.H * HD + (size_t)(kvh * g + v % g) * HD + 64 * half : nullptr;
 #pragma unroll 1
-        for (int c = 0; c < HD; c += 16) {
+        for (int c = 0; c < HD / 2; c += 16) {
             float o[16];
             tmem_ld16(tO + c, o);
             if (dst) {
