@@ -6,11 +6,12 @@
 // contraction (the round's blocks of 16 rows use attention_mma.cu).
 //
 // A CTA owns 128 query vectors: 128 / g positions of one sequence times the g
-// query heads of one KV head.  Query vector v is TMEM lane v; two threads share
-// it, v (warps 0-3) and v + 128 (warps 4-7, the same TMEM lane quadrants): the
-// first takes key columns 0-31 of each tile and O columns 0-63, the second key
-// columns 32-63 and O columns 64-127, and the two exchange their tile maxima
-// through shared memory (a named barrier per warp pair).  The CTA walks the
+// query heads of one KV head.  Query vector v is TMEM lane v; NSPLIT threads
+// share it, v, v + 128, ... (warps q, q + 4, ... use the same TMEM lane
+// quadrant): part i takes key columns [i 64 / NSPLIT, (i + 1) 64 / NSPLIT) of each
+// tile and O columns [i 128 / NSPLIT, (i + 1) 128 / NSPLIT), and the parts
+// exchange their tile maxima through shared memory (a named barrier per lane
+// quadrant).  The CTA walks the
 // 64-key tiles (= cache pages) 0 .. ceil(max position / 64) in order, with a
 // software pipeline per tile t:
 //   - S_{t+1} = Q K_{t+1}^T is issued on the tensor cores before the softmax of
@@ -41,8 +42,10 @@ using namespace tc;
 constexpr int KT = 64;       // keys per tile = cache page
 constexpr int HD = 128;      // head dim
 constexpr int QM = 128;      // query vectors per CTA (MMA M)
-constexpr int NT = 256;      // threads: 8 warps, two per TMEM lane quadrant
-constexpr int KH = KT / 2;   // key columns per thread of a tile
+constexpr int NSPLIT = 4;    // threads per query vector (warps q, q + 4, ... share a TMEM lane quadrant)
+constexpr int NT = 128 * NSPLIT;
+constexpr int KH = KT / NSPLIT;   // key columns per thread of a tile
+constexpr int OH = 128 / NSPLIT;  // O columns per thread
 constexpr int RING = 4;      // K/V ring stages
 
 constexpr int Q_REG = QM * 128;       // 16 KB: one 64-dim half of the 128 query rows
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
     uint64_t* bar_o = bar_s + 2;                                  // P.V complete
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 3);
     __shared__ int glim_s;
-    __shared__ float xch_s[2][QM];  // the two halves of each query vector: tile max, final sum
+    __shared__ float xch_s[NSPLIT][QM];  // the parts of each query vector: tile max, final sum
 
     const AttnParams& p = a.p;
     const int grp = gridDim.x - 1 - blockIdx.x;  // later positions (more key tiles) first
@@ -92,7 +95,7 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
     const int nrows = min(p.group_rows, p.rows - r0);
     const int nv = nrows * g;
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int v = tid & (QM - 1), half = tid >> 7;  // query vector (TMEM lane) and key / O half
+    const int v = tid & (QM - 1), half = tid >> 7;  // query vector (TMEM lane) and its key / O part
     const int seq = p.seq_div > 0 ? r0 / p.seq_div : p.row_seq[r0];
 
     if (warp == 0) {
@@ -111,7 +114,7 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
     fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t t_lane = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t tO = tmem + t_lane + 128 + 64 * half;  // this thread's O columns (of 128 .. 255)
+    const uint32_t tO = tmem + t_lane + 128 + OH * half;  // this thread's O columns (of 128 .. 255)
 
     // causal key limit of this thread's query vector
     int lim = 0;
@@ -120,18 +123,21 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
         if (p.row_seq[r] >= 0) lim = p.row_pos[r] + 1;
     }
     atomicMax(&glim_s, lim);
-    // Q into the swizzled A operand (padding rows zero): each half copies one 64-dim region
+    // Q into the swizzled A operand (padding rows zero): each part copies 16 / NSPLIT of the
+    // row's sixteen 16-byte chunks
     {
+        constexpr int QC = 16 / NSPLIT;
         const uint4* src = nullptr;
         if (v < nv) {
             const int r = r0 + v / g, h = kvh * g + v % g;
             src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + (size_t)r * p.H * HD +
-                                                 (size_t)h * HD) + 8 * half;
+                                                 (size_t)h * HD);
         }
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int i = 0; i < QC; ++i) {
+            const int ch = QC * half + i;
             const uint4 x = src ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sm + Q_OFF + half * Q_REG + swz(v, ch)) = x;
+            *reinterpret_cast<uint4*>(sm + Q_OFF + (ch >> 3) * Q_REG + swz(v, ch & 7)) = x;
         }
     }
     __syncthreads();
@@ -204,19 +210,18 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
         float sc[KH];
         {
             const uint32_t tS = tmem + t_lane + (uint32_t)((it & 1) * KT + KH * half);
-            uint32_t r0_[16], r1_[16];
-            tmem_ld16_issue(tS, r0_);
-            tmem_ld16_issue(tS + 16, r1_);
-            tmem_ld_wait(r0_);
-            tmem_ld_wait(r1_);
+            uint32_t r_[KH / 16][16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                sc[c] = __uint_as_float(r0_[c]);
-                sc[16 + c] = __uint_as_float(r1_[c]);
-            }
+            for (int q = 0; q < KH / 16; ++q) tmem_ld16_issue(tS + 16 * q, r_[q]);
+#pragma unroll
+            for (int q = 0; q < KH / 16; ++q) tmem_ld_wait(r_[q]);
+#pragma unroll
+            for (int q = 0; q < KH / 16; ++q)
+#pragma unroll
+                for (int c = 0; c < 16; ++c) sc[16 * q + c] = __uint_as_float(r_[q][c]);
         }
         // (C) online softmax, lazy reference max (moves only by more than 2^8); the row's
-        // tile max from both halves (warps w and w + 4 meet at named barrier 1 + w % 4)
+        // tile max from all its parts (the warps of quadrant w % 4 meet at named barrier 1 + w % 4)
         float mx = -INFINITY;
         const int k0 = it * KT + KH * half;
 #pragma unroll
@@ -225,9 +230,10 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
             mx = fmaxf(mx, sc[c]);
         }
         xch_s[half][v] = mx;
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
-        mx = fmaxf(mx, xch_s[half ^ 1][v]);
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");  // both read before the next write
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "n"(32 * NSPLIT) : "memory");
+#pragma unroll
+        for (int q = 0; q < NSPLIT; ++q) mx = fmaxf(mx, xch_s[q][v]);
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "n"(32 * NSPLIT) : "memory");  // all read first
         const float m_new = (mx > m_run + 8.f) ? mx : m_run;
         const float alpha = (m_new == m_run) ? 1.f : ((m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new));
         float sum = 0.f;  // this half's share; the halves' running sums are added at the end
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
             fence_after();
         }
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {  // 16-byte chunks 4 half .. 4 half + 3 of row v
+        for (int ch = 0; ch < KH / 8; ++ch) {  // this part's 16-byte chunks of row v
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -252,14 +258,14 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
                 hi[e] = pack2_bf16(x0, x1);
                 lo[e] = pack2_bf16(x0 - __uint_as_float(hi[e] << 16), x1 - __uint_as_float(hi[e] & 0xFFFF0000u));
             }
-            *reinterpret_cast<uint4*>(sm + P_OFF + swz(v, 4 * half + ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(sm + P_OFF + QM * 128 + swz(v, 4 * half + ch)) =
+            *reinterpret_cast<uint4*>(sm + P_OFF + swz(v, (KH / 8) * half + ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(sm + P_OFF + QM * 128 + swz(v, (KH / 8) * half + ch)) =
                 make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         // rescale the running O when the reference max moved (warp-collective TMEM access)
         if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-            for (int c = 0; c < HD / 2; c += 16) {
+            for (int c = 0; c < OH; c += 16) {
                 float o[16];
                 tmem_ld16(tO + c, o);
 #pragma unroll
@@ -296,13 +302,15 @@ __global__ void __launch_bounds__(NT, 1) attn_prefill_tc_kernel(PfArgs a) {
     __syncthreads();
     if (n > 0) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-        const float l = xch_s[0][v] + xch_s[1][v];
+        float l = 0.f;
+#pragma unroll
+        for (int q = 0; q < NSPLIT; ++q) l += xch_s[q][v];
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const bool live = okw && v < nv && lim > 0;
         __nv_bfloat16* dst =
-            live ? out + (size_t)(r0 + v / g) * p.H * HD + (size_t)(kvh * g + v % g) * HD + 64 * half : nullptr;
+            live ? out + (size_t)(r0 + v / g) * p.H * HD + (size_t)(kvh * g + v % g) * HD + OH * half : nullptr;
 #pragma unroll 1
-        for (int c = 0; c < HD / 2; c += 16) {
+        for (int c = 0; c < OH; c += 16) {
             float o[16];
             tmem_ld16(tO + c, o);
             if (dst) {
