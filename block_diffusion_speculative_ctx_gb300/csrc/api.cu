@@ -19,6 +19,7 @@
 
 #include "dflash.h"
 #include "launch.h"
+#include "page_pool.h"
 #include "loss.h"
 
 using namespace dfl;
@@ -83,11 +84,7 @@ struct dflash_ctx {
     // KV page pool (host side): physical pages [0, pool_pages) of the caches, the last one a
     // scratch page that backs every unassigned table entry (never handed out)
     int pool_pages = 0;
-    std::vector<int> free_pages;      // stack of unassigned pages
-    std::vector<int> slot_pages;      // logical pages assigned to each slot
-    std::vector<int> pt_host;         // mirror of page_table
-    bool pt_full = false;             // the whole table must be uploaded (after a reset)
-    std::vector<int> pt_pending;      // table entries assigned since the last upload
+    PagePool pool;
     float2* rope = nullptr;
 
     int R = 0;  // row capacity
@@ -811,60 +808,41 @@ struct Pass {
 
 // ---- KV page pool
 // Every slot's table row returns to the scratch page and every page to the pool.
-void pool_reset(dflash_ctx* c) {
-    const int scratch = c->pool_pages - 1;
-    c->free_pages.clear();
-    for (int p = scratch - 1; p >= 0; --p) c->free_pages.push_back(p);
-    c->slot_pages.assign(c->cfg.max_batch, 0);
-    c->pt_host.assign((size_t)c->cfg.max_batch * c->kv.pages_per_seq, scratch);
-    c->pt_full = true;
-    c->pt_pending.clear();
-}
+void pool_reset(dflash_ctx* c) { c->pool.reset(); }
 
 // Back positions [0, tokens) of `slot` with pages; false when the pool runs out.
-bool pool_ensure(dflash_ctx* c, int slot, long long tokens) {
-    const int pps = c->kv.pages_per_seq;
-    const long long need_ll = (tokens + PAGE_TOKENS - 1) / PAGE_TOKENS;
-    const int need = (int)std::min<long long>(need_ll, pps);
-    while (c->slot_pages[slot] < need) {
-        if (c->free_pages.empty()) return false;
-        const size_t e = (size_t)slot * pps + c->slot_pages[slot]++;
-        c->pt_host[e] = c->free_pages.back();
-        c->free_pages.pop_back();
-        c->pt_pending.push_back((int)e);
-    }
-    return true;
-}
+bool pool_ensure(dflash_ctx* c, int slot, long long tokens) { return c->pool.ensure(slot, tokens, PAGE_TOKENS); }
 
 // The device page table follows the host mirror, in stream order: after a reset the whole table
 // (a pageable copy, which may wait for the stream: prefill, init and the training forward only);
 // between rounds the few new entries, written by a kernel that carries them in its parameters,
 // so that the rounds stay asynchronous.
 dflash_status pool_upload(dflash_ctx* c) {
-    if (c->pt_full) {
-        CUDA_TRY(c, cudaMemcpyAsync(c->page_table, c->pt_host.data(), c->pt_host.size() * 4,
-                                    cudaMemcpyHostToDevice, c->stream));
-        c->pt_full = false;
-        c->pt_pending.clear();
+    const PagePool& P = c->pool;
+    if (P.full_dirty()) {
+        CUDA_TRY(c, cudaMemcpyAsync(c->page_table, P.table().data(), P.table().size() * 4, cudaMemcpyHostToDevice,
+                                    c->stream));
+        c->pool.uploaded();
         return DFLASH_OK;
     }
     Launch L = c->L();
-    for (size_t i = 0; i < c->pt_pending.size(); i += 64) {
+    const std::vector<int>& pend = P.pending();
+    for (size_t i = 0; i < pend.size(); i += 64) {
         PageUpdates u;
-        u.n = (int)std::min<size_t>(64, c->pt_pending.size() - i);
+        u.n = (int)std::min<size_t>(64, pend.size() - i);
         for (int j = 0; j < u.n; ++j) {
-            u.idx[j] = c->pt_pending[i + j];
-            u.page[j] = c->pt_host[c->pt_pending[i + j]];
+            u.idx[j] = pend[i + j];
+            u.page[j] = P.table()[pend[i + j]];
         }
         set_pages(L, c->page_table, u);
     }
-    c->pt_pending.clear();
+    c->pool.uploaded();
     return launch_check(c);
 }
 
 dflash_status pool_full(dflash_ctx* c, int slot, long long tokens) {
     return c->fail(DFLASH_E_CAPACITY, "KV page pool exhausted: sequence %d needs %lld tokens (%d pages of %d in use)",
-                   slot, tokens, c->pool_pages - 1 - (int)c->free_pages.size(), c->pool_pages - 1);
+                   slot, tokens, c->pool.in_use(), c->pool.capacity());
 }
 
 dflash_status capacity_check(dflash_ctx* c) {
@@ -1141,7 +1119,7 @@ dflash_status dflash_init(const dflash_config* cfg, const dflash_weights* w, voi
     ALLOC(c->dK, (size_t)c->Ld * c->kv.layer_stride * esz);
     ALLOC(c->dV, (size_t)c->Ld * c->kv.layer_stride * esz);
     ALLOC(c->page_table, table * 4);
-    pool_reset(c);
+    c->pool.init(c->pool_pages, cfg->max_batch, c->kv.pages_per_seq);
     if (pool_upload(c) != DFLASH_OK || cudaStreamSynchronize(c->stream) != cudaSuccess) {
         c->fail(DFLASH_E_CUDA, "page table upload failed");
         return bail(DFLASH_E_CUDA);
@@ -1443,11 +1421,9 @@ dflash_status dflash_train_forward(dflash_ctx* c, int32_t n_tokens, const int32_
     if (s) return s;
     // 2. slot i+1 shares slot 0's pages below its anchor's page and takes its own pages from the
     //    pool for the rest of its block
-    const int pps = c->kv.pages_per_seq;
     for (int i = 0; i < m; ++i) {
         const int p0 = anchors[i] >> PAGE_SHIFT;
-        for (int t = 0; t < p0; ++t) c->pt_host[(size_t)(i + 1) * pps + t] = c->pt_host[t];
-        c->slot_pages[i + 1] = p0;
+        c->pool.share(i + 1, 0, p0);
         if (!pool_ensure(c, i + 1, (long long)anchors[i] + B)) {
             const dflash_status st = pool_full(c, i + 1, (long long)anchors[i] + B);
             pool_reset(c);
@@ -1463,9 +1439,9 @@ dflash_status dflash_train_forward(dflash_ctx* c, int32_t n_tokens, const int32_
     for (int l = 0; l < c->Ld; ++l)
         for (int i = 0; i < m; ++i) {
             const int p0 = anchors[i] >> PAGE_SHIFT;
-            const size_t src = (size_t)l * c->kv.layer_stride + (size_t)c->pt_host[p0] * page_elems;
+            const size_t src = (size_t)l * c->kv.layer_stride + (size_t)c->pool.page(0, p0) * page_elems;
             const size_t dst =
-                (size_t)l * c->kv.layer_stride + (size_t)c->pt_host[(size_t)(i + 1) * pps + p0] * page_elems;
+                (size_t)l * c->kv.layer_stride + (size_t)c->pool.page(i + 1, p0) * page_elems;
             CUDA_TRY(c, cudaMemcpyAsync((char*)c->dK + dst * c->esz, (char*)c->dK + src * c->esz, page_elems * c->esz,
                                         cudaMemcpyDeviceToDevice, c->stream));
             CUDA_TRY(c, cudaMemcpyAsync((char*)c->dV + dst * c->esz, (char*)c->dV + src * c->esz, page_elems * c->esz,
@@ -1575,7 +1551,6 @@ dflash_status dflash_inspect(dflash_ctx* c, int32_t what, int32_t seq, int32_t l
                              size_t* written) {
     if (!c || !dst) return DFLASH_E_INVAL;
     size_t need = 0;
-    const void* src = nullptr;
     const int b = c->batch, B = c->B;
     auto simple = [&](const void* p, size_t n) -> dflash_status {
         if (bytes < n) return c->fail(DFLASH_E_INVAL, "buffer of %zu bytes, need %zu", bytes, n);
@@ -1649,7 +1624,6 @@ dflash_status dflash_inspect(dflash_ctx* c, int32_t what, int32_t seq, int32_t l
         }
         default: return c->fail(DFLASH_E_INVAL, "unknown inspect item %d", what);
     }
-    (void)src;
 }
 
 dflash_status dflash_set_profiling(dflash_ctx* c, int32_t on) {
