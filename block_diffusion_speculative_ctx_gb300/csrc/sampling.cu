@@ -692,12 +692,14 @@ __global__ void __launch_bounds__(SNT) row_nll_kernel(const float* __restrict__ 
 
 }  // namespace
 
-int law_cluster_size(int V) {
+// CTAs per law row: one per 8192 tokens, at most a portable cluster of 8.
+static int law_cluster_size(int V) {
     const int nc = (V + 8191) / 8192;
     return nc < 1 ? 1 : (nc > MAX_NC ? MAX_NC : nc);
 }
 
-size_t law_smem_bytes(int V) {
+// Dynamic shared memory of a law CTA: two radix histograms and the staged chunk of keys.
+static size_t law_smem_bytes(int V) {
     const int nc = law_cluster_size(V);
     const size_t C = ((size_t)(V + nc - 1) / nc + 3) / 4 * 4;
     return 2 * HB * sizeof(unsigned long long) + C * sizeof(float);
