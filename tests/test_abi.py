@@ -86,6 +86,8 @@ def _valid_cfg():
     ("d_model", 200, "d_model"),
     ("dtype", 7, "dtype"),
     ("max_batch", 0, "max_batch"),
+    ("kv_pool_tokens", -64, "kv_pool_tokens"),
+    ("kv_pool_tokens", 1 << 40, "kv_pool_tokens"),
 ])
 def test_init_rejects_bad_configs_without_touching_the_gpu(lib, field, value, needle):
     cfg = _valid_cfg()
@@ -119,5 +121,6 @@ def test_null_arguments(lib):
     assert lib.dflash_draft_block_sampled(None, 1.0, None, None) == dfl.DFLASH_E_INVAL
     assert lib.dflash_verify_sampled(None, 1.0, None, None, None, None) == dfl.DFLASH_E_INVAL
     assert lib.dflash_set_block_size(None, 4) == dfl.DFLASH_E_INVAL
+    assert lib.dflash_set_sampling_filter(None, 0, 1.0) == dfl.DFLASH_E_INVAL
     assert lib.dflash_block_size(None) == -1
     lib.dflash_destroy(None)
